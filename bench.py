@@ -1,0 +1,430 @@
+"""Benchmark: one decode step (paged KV append + paged decode attention) of one layer.
+
+Default workload: the Llama-3-8B-shaped decode layer (batch 64, context lengths uniform
+in [512, 4096], Hq 32 / Hkv 8, D 128, 16-token blocks, bf16 KV, shuffled pool, 64 new
+tokens appended before attention).  Every value is seeded synthetic data.
+
+Metric: achieved HBM GB/s of the step = algorithmic bytes / device time, where the
+algorithmic bytes are the unique valid KV bytes the attention must read (shared blocks
+once) plus q, the output, the block tables and lengths, and the append's reads and writes.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+Under torchrun each rank runs its own replica (independent sequences, no collective on the
+data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention achieved HBM GB/s (fraction of 8 TB/s); µs/decode step"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20  # about twice the 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="llama3_8b", choices=W.ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------ byte accounting
+
+def step_bytes(w: W.Workload) -> dict:
+    """Algorithmic bytes of one step (the roofline numerator)."""
+    c = w.cfg
+    B = w.batch
+    kv = w.unique_kv_bytes()
+    q = B * c.hq * c.d * 2
+    out = B * c.hq * c.d * 2
+    meta = sum((s.length + 15) // 16 for s in w.seqs) * 4 + B * 4 + (2 * c.hkv * 4 if w.scales is not None else 0)
+    T = w.slot_mapping.numel()
+    append = T * c.hkv * c.d * 2 * 2 + T * c.hkv * c.d * c.elem_bytes * 2 + T * 8
+    decode = kv + q + out + meta
+    return {"decode": decode, "append": append, "step": decode + append, "unique_kv": kv,
+            "logical_kv": w.logical_kv_bytes()}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {}
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_17_gb300", "csrc")
+    for name in ("decode_kernel.cuh", "pkv_device.cuh", "decode_launch.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config: str):
+    """DRAM bytes per decode launch from the committed ncu summary of this workload, if it
+    was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"decode_{config}_ncu.md")
+    if not os.path.exists(p):
+        return None
+    digest, traffic = None, None
+    with open(p) as f:
+        for line in f:
+            if line.startswith("kernel_source_digest:"):
+                digest = line.split(":", 1)[1].strip()
+            if line.startswith("dram_bytes_per_launch:"):
+                traffic = int(line.split(":", 1)[1].strip())
+    return traffic if digest == kernel_source_digest() else None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        top = max(sms)
+        loaded = [s for s in sms if s >= 0.5 * top] or sms
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# ------------------------------------------------------------------ CPU baseline (the oracle)
+
+def oracle_sample(w: W.Workload, budget_s: float, threads: int):
+    """Time the fp64 CPU oracle on whole (sequence, kv head) groups of this workload -- a
+    prefix of the groups if the whole step takes longer than budget_s, else whole steps
+    repeated until about budget_s seconds; returns (GB/s of unique KV, seconds,
+    description, bytes)."""
+    import oracle
+
+    a = w.np()
+    c = w.cfg
+    g = c.g
+    per_tok = 2 * c.d * c.elem_bytes  # K+V bytes of one token of one kv head
+    b0 = 0
+    pairs = np.array([(b0, hq) for hq in range(g)], dtype=np.int32)
+    t0 = time.perf_counter()
+    oracle.decode_pairs(a["q"], a["k_cache"], a["v_cache"], w.kv_dtype_code, a["block_tables"], a["context_lens"],
+                        c.softmax_scale, pairs, scales=a["scales"], nthreads=1)
+    sec_per_tok = (time.perf_counter() - t0) / max(1, w.seqs[b0].length)
+    target_tok = budget_s * threads / max(sec_per_tok, 1e-12)
+    groups, tok = [], 0
+    for b in range(w.batch):
+        for h in range(c.hkv):
+            if tok >= target_tok:
+                break
+            groups.append((b, h))
+            tok += w.seqs[b].length
+    pairs = np.array([(b, h * g + i) for (b, h) in groups for i in range(g)], dtype=np.int32)
+    reps, dt = 0, 0.0
+    while True:
+        t0 = time.perf_counter()
+        oracle.decode_pairs(a["q"], a["k_cache"], a["v_cache"], w.kv_dtype_code, a["block_tables"],
+                            a["context_lens"], c.softmax_scale, pairs, scales=a["scales"], nthreads=threads)
+        dt += time.perf_counter() - t0
+        reps += 1
+        if dt >= 0.8 * budget_s or len(groups) < w.batch * c.hkv:
+            break
+    nbytes = tok * per_tok * reps
+    whole = len(groups) == w.batch * c.hkv
+    desc = (f"{'the whole step' if whole else f'{len(groups)} of {w.batch * c.hkv} (sequence, kv head) groups'}"
+            f" x {reps} ({tok} tokens, {tok * per_tok / 1e6:.1f} MB of KV per pass), all {g} query heads of "
+            f"each group; fp64 C oracle on {threads} threads")
+    return nbytes / dt / 1e9, dt, desc, nbytes
+
+
+def host_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import paged_kv_cache_17_gb300 as pkv
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg = W.get(args.config)
+    w = W.make_workload(cfg, seed=cfg.seed + 1000 * rank)
+    nb = step_bytes(w)
+    B, hq, hkv, d = w.batch, cfg.hq, cfg.hkv, cfg.d
+    max_len = int(w.context_lens.max())
+    t = {k: (v.to(dev) if v is not None else None) for k, v in
+         dict(q=w.q, k_cache=w.k_cache, v_cache=w.v_cache, k_new=w.k_new, v_new=w.v_new, slots=w.slot_mapping,
+              tables=w.block_tables, lens=w.context_lens, scales=w.scales).items()}
+    out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=dev)
+    need = pkv.workspace_size(B, hq, hkv, d, max_len)
+    wsbuf = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        pkv.paged_kv_append(t["k_new"], t["v_new"], t["slots"], t["k_cache"], t["v_cache"], scales=t["scales"])
+        mid.record(stream)
+        pkv.paged_decode_attention(t["q"], t["k_cache"], t["v_cache"], t["tables"], t["lens"], cfg.softmax_scale,
+                                   out, scales=t["scales"], max_context_len=max_len, workspace=wsbuf)
+
+    mid = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    assert pkv.check_device_status() == 0
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)  # evict the previous step's lines from L2 (not timed)
+            e0, e1, e2 = evs[i]
+            e0.record(stream)
+            mid = e1
+            step()
+            e2.record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        wall = time.perf_counter() - wall0
+    clocks = clk.summary()
+    if clocks.get("samples", 0) < 3:
+        # the timed region was shorter than the sampler's period: sample the same step loop
+        # for another half second (untimed) and say so
+        mid = torch.cuda.Event(enable_timing=True)  # keep the timed events untouched
+        with ClockSampler(dev.index) as clk2:
+            t_end = time.perf_counter() + 0.5
+            while time.perf_counter() < t_end:
+                for _ in range(50):
+                    flush.fill_(3)
+                    step()
+                torch.cuda.synchronize()
+        clocks = clk2.summary()
+        clocks["window"] = "same step loop, 0.5 s right after the timed region (timed region too short)"
+    else:
+        clocks["window"] = "timed region"
+    step_ms = [e0.elapsed_time(e2) for (e0, e1, e2) in evs]
+    dec_ms = [e1.elapsed_time(e2) for (e0, e1, e2) in evs]
+    tot_ms = sum(step_ms)
+    if ws > 1:
+        tt = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        tot_ms = float(tt.item())
+    assert pkv.check_device_status() == 0
+    value = nb["step"] * ws * args.steps / (tot_ms * 1e-3) / 1e9
+    ms_per_step = tot_ms / args.steps
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    achieved = nb["decode"] / (dec_avg_ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or FALLBACK_HBM_GBS
+
+    # ---- end to end through the public API with host buffers (pinned), H2D + D2H timed
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.pin_memory() for k, v in dict(q=w.q, k_new=w.k_new, v_new=w.v_new, slots=w.slot_mapping,
+                                                     tables=w.block_tables, lens=w.context_lens).items()}
+        h_out = torch.empty((B, hq, d), dtype=torch.bfloat16).pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            for k, v in host.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            pkv.paged_kv_append(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], t["k_cache"], t["v_cache"],
+                                scales=t["scales"])
+            pkv.paged_decode_attention(dev_in["q"], t["k_cache"], t["v_cache"], dev_in["tables"], dev_in["lens"],
+                                       cfg.softmax_scale, out, scales=t["scales"], max_context_len=max_len,
+                                       workspace=wsbuf)
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            ee[i][0].record(stream)
+            e2e_step()
+            ee[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
+        if ws > 1:
+            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": round(nb["step"] * ws * args.steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_ms / args.steps, 4)}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        thr = host_threads()
+        gbs, dt, desc, _ = oracle_sample(w, args.cpu_seconds, thr)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc,
+               "seconds": round(dt, 2)}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.kv_dtype == "bf16" else "e4m3",
+        "data": "synthetic (seeded N(0,1) bf16 q/K/V, shuffled 16-token block pool)",
+        "config": {"workload": f"{cfg.name}: batch {B}, context {cfg.len_range if cfg.kind == 'uniform' else 'mixed'}, "
+                               f"Hq {hq}, Hkv {hkv}, D {d}, block 16, {cfg.kv_dtype} KV, append {w.slot_mapping.numel()} tokens",
+                   "batch": B, "num_q_heads": hq, "num_kv_heads": hkv, "head_dim": d, "kv_dtype": cfg.kv_dtype,
+                   "max_context_len": max_len, "total_context_tokens": w.total_tokens(),
+                   "partition_tokens": pkv.partition_tokens(B, hkv, max_len),
+                   "l2": "flushed between timed steps (256 MiB write, untimed)", "parallelism": f"replicas x{ws}"},
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
+        "bytes_per_step": nb,
+        "decode_us": round(dec_avg_ms * 1e3, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(cfg.name),
+                     "kernel": "paged_decode_kernel", "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "wall_s": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return  # the oracle runs on rank 0 only
+    cfg = W.get(args.config)
+    w = W.make_workload(cfg)
+    thr = host_threads()
+    per_step = max(1.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step, thr)
+    total_b, total_s, desc = 0, 0.0, ""
+    for _ in range(args.steps):
+        _, dt, desc, nbytes = oracle_sample(w, per_step, thr)
+        total_b += nbytes
+        total_s += dt
+    value = total_b / total_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": cfg.name},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        import __graft_entry__
+
+        __graft_entry__.build()
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache decode library (GB300, sm_103a).
+ *
+ * Two operations make up one decode step of one attention layer over a block-paged
+ * KV cache:
+ *
+ *   pkv_paged_kv_append         scatter the step's new K/V rows into the pool
+ *   pkv_paged_decode_attention  one query vector per sequence attends over that
+ *                               sequence's cached K/V, gathered through its block table
+ *
+ * Sources (page title, section):
+ *   habr.com/ru/articles/1021832 ("KV-Cache ... в рамках одного GPU"):
+ *     section 1 "Prefill и Decode"  -- decode appends one new K,V per step ("append");
+ *     section 2 "KV-Cache: цена памяти" -- bytes/token formula, GQA (query heads
+ *        sharing a KV head), FP8 KV cache (--kv-cache-dtype fp8);
+ *     section 3 "Вспомним FlashAttention" -- Attention(Q,K,V) = softmax(QK^T/sqrt(d_k))V,
+ *        computed tile by tile with a running max and running sum, exactly;
+ *     section 4 "Вспомним PagedAttention" -- 16-token blocks, block table as a page
+ *        table, blocks scattered in GPU memory, worked example of slot assignment;
+ *     section 5 "Как vLLM объединяет FlashAttention и PagedAttention" -- the decode call
+ *        flash_attn_with_kvcache(q [batch,1,num_heads,d_head],
+ *        k_cache/v_cache [num_physical_blocks, block_size, num_kv_heads, d_head],
+ *        block_table [batch, max_num_blocks] int32, cache_seqlens [batch]).
+ *   actionbridge.io ... chapter 8 "KV cache management" -- flat physical pool, the
+ *     attention kernel gathers keys and values through the block table.
+ *
+ * Conventions shared by every call
+ *   - All data pointers are DEVICE pointers on the current CUDA device, owned by the
+ *     caller.  The library allocates no device or pinned memory and keeps no state
+ *     except cached device properties, a cached driver entry point, a device status
+ *     word (see pkv_check_device_status) and a thread-local error string.
+ *   - Calls enqueue work on `stream` and return without synchronising.  A NULL stream
+ *     is the legacy default stream.
+ *   - Host-side validation runs before anything is enqueued; on failure nothing is
+ *     enqueued and the call returns PKV_ERR_INVALID_ARG / PKV_ERR_UNSUPPORTED /
+ *     PKV_ERR_WORKSPACE with a message in pkv_last_error().  A failed launch returns
+ *     PKV_ERR_CUDA.  No C++ exception crosses this interface.
+ *   - Data-dependent checks run on the device without faulting: a slot outside the
+ *     pool, a block id outside the pool, a context length outside
+ *     [0, min(max_context_len, max_blocks_per_seq*16)] are skipped or clamped, and a
+ *     bit is set in the device status word, which pkv_check_device_status reports.
+ *     Reads through an out-of-range block id return zeros (the tensor-map bounds of the
+ *     pool), never memory outside it.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream, declared here so C callers need no CUDA header. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,  /* bad pointer, shape, alignment or size */
+  PKV_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head_dim, group size, device) */
+  PKV_ERR_WORKSPACE = 3,    /* workspace missing or smaller than pkv_decode_workspace_size() */
+  PKV_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  PKV_ERR_DEVICE_CHECK = 5  /* pkv_check_device_status found a device-side check failure */
+} pkv_status;
+
+typedef enum {
+  PKV_KV_BF16 = 0,     /* pool elements are bf16 */
+  PKV_KV_FP8_E4M3 = 1  /* pool elements are OCP E4M3 bytes with per-(K|V, kv head) fp32 scales */
+} pkv_kv_dtype;
+
+typedef enum { PKV_OUT_BF16 = 0, PKV_OUT_FP32 = 1 } pkv_out_dtype;
+
+/* Device status word bits (pkv_check_device_status). */
+#define PKV_DEVFLAG_BAD_SLOT 0x1u        /* append: slot >= num_blocks * block_size (skipped) */
+#define PKV_DEVFLAG_BAD_CONTEXT_LEN 0x2u /* decode: context length out of range (clamped) */
+#define PKV_DEVFLAG_BAD_BLOCK_ID 0x4u    /* decode: block id outside the pool (read as zeros) */
+#define PKV_DEVFLAG_WAIT_TIMEOUT 0x8u    /* decode: a pipeline wait hit its iteration limit */
+
+/*
+ * The caller-owned paged pool.  Nothing is copied; the struct is read during the call.
+ *   k_cache, v_cache: [num_blocks][block_size][num_kv_heads][head_dim], row-major,
+ *     elements bf16 (2 bytes) or E4M3 (1 byte) -- the layout of section 5 above.
+ *     Both must be 16-byte aligned.  num_blocks * block_size must fit in int32.
+ *   block_size: must be 16 (section 4: "по умолчанию — 16").
+ *   head_dim: 64 or 128.
+ *   scales: for PKV_KV_FP8_E4M3, device fp32 [2][num_kv_heads] -- row 0 scales K, row 1
+ *     scales V; a stored code c means the value decode(c) * scale.  NULL for bf16.
+ */
+typedef struct {
+  void* k_cache;
+  void* v_cache;
+  int64_t num_blocks;
+  int32_t block_size;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  pkv_kv_dtype kv_dtype;
+  const float* scales;
+} pkv_cache_desc;
+
+/*
+ * Append one step's new K/V rows (section 1 "append", section 4 worked example: token
+ * 1025 goes to the next free slot of the sequence's current block).
+ *   k, v: [num_tokens][num_kv_heads][head_dim] bf16, 16-byte aligned.
+ *   slot_mapping: [num_tokens] int64; slot = physical_block * block_size + offset.
+ *     slot < 0 skips the token (padding).  slot >= num_blocks*block_size is skipped and
+ *     sets PKV_DEVFLAG_BAD_SLOT.
+ *   For every kept token t, head h, element i:
+ *     cache[slot / block_size][slot % block_size][h][i] = enc(x[t][h][i])
+ *   where enc is a bit copy for bf16, and for E4M3 the binary32 division x / scale
+ *   (scale = scales[0][h] for K, scales[1][h] for V) rounded to nearest-even E4M3 and
+ *   saturated to +-448.
+ *   Two tokens with the same slot: which one lands is unspecified.
+ *   num_tokens == 0 is a no-op returning PKV_OK.
+ */
+pkv_status pkv_paged_kv_append(const pkv_cache_desc* cache, const void* k, const void* v,
+                               const int64_t* slot_mapping, int64_t num_tokens,
+                               pkv_stream_t stream);
+
+/*
+ * Bytes of device workspace that pkv_paged_decode_attention needs for these sizes on the
+ * current device (0 if the call needs none, i.e. when no sequence is split).  The workspace
+ * holds per-partition partial results (running max, running sum, unnormalised output) of
+ * the context split, after a ticket region of fixed size (pkv_decode_workspace_tickets_bytes)
+ * holding one int32 ticket per (sequence, kv head).
+ * Contract: the ticket region must be zero before the first call that uses a workspace
+ * (zero the whole buffer once when allocating it); every call that completes leaves it zero
+ * again, whatever the sizes of the next call.  A workspace may not be used by two calls
+ * that can run at the same time.
+ * Returns 0 and sets pkv_last_error() for invalid sizes.
+ */
+size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t max_context_len);
+
+/* Size of the ticket region at the start of every non-empty workspace (a constant). */
+size_t pkv_decode_workspace_tickets_bytes(void);
+
+/* Context partition length (tokens, a multiple of 16) the decode uses for these sizes on
+ * the current device; a sequence of n tokens is split into ceil(n / partition) parts. */
+int32_t pkv_decode_partition_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_context_len);
+
+/*
+ * Paged decode attention (section 3 definition, section 5 call shape, GQA of section 2).
+ *   q: [batch][num_q_heads][head_dim] bf16, 16-byte aligned.
+ *   block_tables: [batch][max_blocks_per_seq] int32 physical block ids, row-major.  Only
+ *     the first ceil(context_lens[b] / 16) entries of row b are read.
+ *   context_lens: [batch] int32, the number of cached tokens of each sequence (including
+ *     a token appended this step).  0 gives an all-zero output row.
+ *   max_context_len: an upper bound on every context_lens[b]; it sizes the launch.
+ *   softmax_scale: multiplies q.k before the softmax (1/sqrt(head_dim) in section 3).
+ *   out: [batch][num_q_heads][head_dim], bf16 (round to nearest even) or fp32.
+ *   Query head hq reads kv head hq / (num_q_heads / num_kv_heads); num_q_heads must be a
+ *   multiple of num_kv_heads with a quotient in {1, 2, 4, 8}.
+ *   For each (b, hq), with n = context_lens[b]:
+ *     out[b][hq] = sum_t softmax_t(scale * q[b][hq] . K_t) V_t,  t = 0 .. n-1,
+ *   K_t/V_t the cached rows of kv head hq/G at position t (decoded times its scale for
+ *   E4M3).  The result is deterministic: it depends only on the values, the lengths and
+ *   the partition length, not on physical block ids, batch order or timing.
+ *   workspace: device memory of at least pkv_decode_workspace_size(...) bytes, 256-byte
+ *   aligned, with its ticket region zero on first use (see above); may be NULL when the
+ *   required size is 0.
+ */
+pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t batch,
+                                      int32_t num_q_heads, int32_t max_context_len,
+                                      float softmax_scale, void* out, pkv_out_dtype out_dtype,
+                                      void* workspace, size_t workspace_bytes,
+                                      pkv_stream_t stream);
+
+/*
+ * Read and clear the device status word of the current device after the work queued on
+ * `stream` so far has finished (this call synchronises `stream`).  *flags receives the
+ * PKV_DEVFLAG_* bits (may be NULL).  Returns PKV_ERR_DEVICE_CHECK if any bit was set,
+ * PKV_OK if none, PKV_ERR_CUDA if reading it failed.
+ */
+pkv_status pkv_check_device_status(pkv_stream_t stream, uint32_t* flags);
+
+/* Static description of a status code. */
+const char* pkv_status_string(pkv_status s);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* pkv_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,81 @@
+// decode_launch.cuh -- launch of one decode-kernel instantiation (shared by the TUs that
+// instantiate the bf16 and the E4M3 variants, and by the C-ABI layer that picks one).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "decode_kernel.cuh"
+
+namespace pkv {
+
+// Consumer warps and ring depth of each variant: 4 consumer warps + 1 producer warp,
+// and as many stages as fit in 64 KiB (4..16), so that two to three CTAs share an SM.
+template <int D, bool FP8>
+struct DecodeShape {
+  static constexpr int kNWC = 4;
+  static constexpr int kTile = 16 * D * (FP8 ? 1 : 2);
+  static constexpr int kStagesRaw = 65536 / (2 * kTile);
+  static constexpr int kStages = kStagesRaw < 4 ? 4 : (kStagesRaw > 16 ? 16 : kStagesRaw);
+};
+
+struct DecodeLaunchInfo {
+  int threads;
+  int smem_bytes;
+  int tile_area_bytes;  // bytes usable by the cross-partition merge weights
+};
+
+template <int D, int G, bool FP8>
+DecodeLaunchInfo decode_launch_info() {
+  using S = DecodeShape<D, FP8>;
+  using C = DecodeCfg<D, G, FP8, S::kNWC, S::kStages>;
+  return DecodeLaunchInfo{C::kThreads, C::kSmemBytes, C::kTilesBytes};
+}
+
+template <int D, int G, bool FP8>
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, dim3 grid,
+                          cudaStream_t stream, int device) {
+  using S = DecodeShape<D, FP8>;
+  using C = DecodeCfg<D, G, FP8, S::kNWC, S::kStages>;
+  auto kern = paged_decode_kernel<D, G, FP8, S::kNWC, S::kStages>;
+  static bool configured[64] = {};
+  if (device >= 0 && device < 64 && !configured[device]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[device] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+// Explicit instantiations live in decode_bf16.cu / decode_e4m3.cu.
+#define PKV_DECLARE_DECODE(D, G, FP8)                                                                  \
+  extern template DecodeLaunchInfo decode_launch_info<D, G, FP8>();                                    \
+  extern template cudaError_t launch_decode<D, G, FP8>(const CUtensorMap&, const CUtensorMap&,        \
+                                                       const DecodeParams&, dim3, cudaStream_t, int);
+#define PKV_DEFINE_DECODE(D, G, FP8)                                                             \
+  template DecodeLaunchInfo decode_launch_info<D, G, FP8>();                                     \
+  template cudaError_t launch_decode<D, G, FP8>(const CUtensorMap&, const CUtensorMap&,         \
+                                                const DecodeParams&, dim3, cudaStream_t, int);
+
+#define PKV_FOR_EACH_GROUP(M, D, FP8) M(D, 1, FP8) M(D, 2, FP8) M(D, 4, FP8) M(D, 8, FP8)
+
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, false)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, false)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, true)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, true)
+
+// append (append.cu)
+cudaError_t launch_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                          int hkv, int d, bool fp8, void* k_cache, void* v_cache, int64_t pool_slots,
+                          const float* scales, uint32_t* status, cudaStream_t stream);
+
+}  // namespace pkv

@@ -1,0 +1,397 @@
+// pkv_api.cu -- the C ABI (include/pkv.h): argument checks, the context-partition choice,
+// TMA tensor maps over the caller's pool, the device status word and kernel dispatch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/pkv.h"
+#include "decode_launch.cuh"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+constexpr int kMaxDevices = 64;
+constexpr int kMinSplitBlocks = 16;  // a context partition covers at least 256 tokens
+// The workspace starts with a ticket region of fixed size, so a workspace reused for other
+// sizes never finds partial results of an earlier call where tickets are expected.  Launches
+// with more (sequence, kv head) units than tickets do not split the context: they already
+// have enough CTAs without it.
+constexpr long long kTickets = 65536;
+
+__device__ uint32_t g_pkv_status;  // PKV_DEVFLAG_* bits, one word per device
+
+thread_local std::string t_last_error;
+
+pkv_status fail(pkv_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+pkv_status fail(pkv_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  uint32_t* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+pkv_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!d.ready) {
+      if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+      cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+      cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_pkv_status)) != cudaSuccess)
+        return cuda_fail(e, "cudaGetSymbolAddress(status)");
+      d.status = static_cast<uint32_t*>(p);
+      if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void* fn = nullptr;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+          return fail(PKV_ERR_CUDA, "driver entry point cuTensorMapEncodeTiled unavailable");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+      }
+      d.ready = true;
+    }
+  }
+  if (d.cc_major != 10 || d.cc_minor != 3)
+    return fail(PKV_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", d.cc_major, d.cc_minor);
+  *out = &d;
+  return PKV_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+pkv_status check_cache(const pkv_cache_desc* c) {
+  if (!c) return fail(PKV_ERR_INVALID_ARG, "cache descriptor is NULL");
+  if (!c->k_cache || !c->v_cache) return fail(PKV_ERR_INVALID_ARG, "k_cache / v_cache is NULL");
+  if (!aligned(c->k_cache, 16) || !aligned(c->v_cache, 16))
+    return fail(PKV_ERR_INVALID_ARG, "k_cache / v_cache must be 16-byte aligned");
+  if (c->block_size != 16) return fail(PKV_ERR_UNSUPPORTED, "block_size must be 16 (got %d)", c->block_size);
+  if (c->num_kv_heads <= 0) return fail(PKV_ERR_INVALID_ARG, "num_kv_heads must be positive");
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", c->head_dim);
+  if (c->num_blocks <= 0) return fail(PKV_ERR_INVALID_ARG, "num_blocks must be positive");
+  if (c->num_blocks * 16 > 0x7fffffffLL) return fail(PKV_ERR_INVALID_ARG, "num_blocks * 16 must fit in int32");
+  if (c->kv_dtype != PKV_KV_BF16 && c->kv_dtype != PKV_KV_FP8_E4M3)
+    return fail(PKV_ERR_INVALID_ARG, "unknown kv_dtype %d", static_cast<int>(c->kv_dtype));
+  if (c->kv_dtype == PKV_KV_FP8_E4M3 && !c->scales)
+    return fail(PKV_ERR_INVALID_ARG, "an E4M3 pool needs scales [2][num_kv_heads]");
+  if (c->kv_dtype == PKV_KV_BF16 && c->scales) return fail(PKV_ERR_INVALID_ARG, "a bf16 pool takes no scales");
+  if (c->scales && !aligned(c->scales, 4)) return fail(PKV_ERR_INVALID_ARG, "scales must be 4-byte aligned");
+  return PKV_OK;
+}
+
+// ---------------------------------------------------------------- context partitions
+
+struct Split {
+  int split_blocks;
+  int max_splits;
+};
+
+// Partitions of equal logical length (a multiple of 16 tokens) so that a batch at its
+// maximal length spreads over about four CTAs per SM slot; never shorter than 256 tokens.
+// PKV_SPLIT_TOKENS (a positive multiple of 16) overrides the choice, for tuning and tests.
+Split choose_split(int batch, int hkv, int max_context_len, int sm_count) {
+  const int max_nblk = (max_context_len + 15) / 16;
+  Split r{1, 1};
+  if (max_nblk <= 0) return r;
+  if (static_cast<long long>(batch) * hkv > kTickets) {
+    r.split_blocks = max_nblk;
+    return r;
+  }
+  int sb = 0;
+  if (const char* env = std::getenv("PKV_SPLIT_TOKENS")) {
+    const long v = std::strtol(env, nullptr, 10);
+    if (v >= 16) sb = static_cast<int>(v / 16);
+  }
+  if (sb == 0) {
+    const long long units = static_cast<long long>(batch) * hkv;
+    const long long target = 4LL * sm_count * 2;  // ~two resident CTAs per SM, four waves
+    long long splits = (target + units - 1) / units;
+    if (splits < 1) splits = 1;
+    sb = static_cast<int>((max_nblk + splits - 1) / splits);
+    if (sb < kMinSplitBlocks) sb = kMinSplitBlocks;
+    sb = (sb + 3) / 4 * 4;
+  }
+  if (sb > max_nblk) sb = max_nblk;
+  r.split_blocks = sb;
+  r.max_splits = (max_nblk + sb - 1) / sb;
+  return r;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct WsLayout {
+  size_t tickets, ml, acc, total;
+};
+
+WsLayout ws_layout(int batch, int hkv, int g, int d, const Split& sp) {
+  WsLayout w{0, 0, 0, 0};
+  if (sp.max_splits <= 1) return w;
+  const size_t units = static_cast<size_t>(batch) * hkv;
+  w.tickets = static_cast<size_t>(kTickets) * sizeof(int32_t);
+  w.ml = round256(units * sp.max_splits * g * 2 * sizeof(float));
+  w.acc = round256(units * sp.max_splits * g * d * sizeof(float));
+  w.total = w.tickets + w.ml + w.acc;
+  return w;
+}
+
+// Merge weights of one (b, h) use G * max_splits + G floats of the tile area.
+Split fit_split(Split sp, int g, int max_context_len, int tile_area_bytes) {
+  const int max_nblk = (max_context_len + 15) / 16;
+  while (sp.max_splits > 1 && static_cast<long long>(g) * (sp.max_splits + 1) * 4 > tile_area_bytes) {
+    sp.split_blocks *= 2;
+    if (sp.split_blocks > max_nblk) sp.split_blocks = max_nblk;
+    sp.max_splits = (max_nblk + sp.split_blocks - 1) / sp.split_blocks;
+  }
+  return sp;
+}
+
+bool encode_kv_map(CUtensorMap* tm, void* base, int64_t num_blocks, int hkv, int d, bool fp8) {
+  const cuuint64_t esz = fp8 ? 1 : 2;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                              static_cast<cuuint64_t>(num_blocks) * 16};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz, static_cast<cuuint64_t>(hkv) * d * esz};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(tm, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base,
+                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+using LaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const pkv::DecodeParams&, dim3, cudaStream_t,
+                                 int);
+using InfoFn = pkv::DecodeLaunchInfo (*)();
+
+struct Variant {
+  LaunchFn launch;
+  InfoFn info;
+};
+
+template <int D, bool FP8>
+Variant pick_g(int g) {
+  switch (g) {
+    case 1: return {pkv::launch_decode<D, 1, FP8>, pkv::decode_launch_info<D, 1, FP8>};
+    case 2: return {pkv::launch_decode<D, 2, FP8>, pkv::decode_launch_info<D, 2, FP8>};
+    case 4: return {pkv::launch_decode<D, 4, FP8>, pkv::decode_launch_info<D, 4, FP8>};
+    case 8: return {pkv::launch_decode<D, 8, FP8>, pkv::decode_launch_info<D, 8, FP8>};
+    default: return {nullptr, nullptr};
+  }
+}
+
+Variant pick_variant(int d, bool fp8, int g) {
+  if (d == 64) return fp8 ? pick_g<64, true>(g) : pick_g<64, false>(g);
+  return fp8 ? pick_g<128, true>(g) : pick_g<128, false>(g);
+}
+
+}  // namespace
+
+// ==================================================================== C ABI
+
+extern "C" {
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_DEVICE_CHECK: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+const char* pkv_last_error(void) { return t_last_error.c_str(); }
+
+int32_t pkv_version(void) { return kVersion; }
+
+pkv_status pkv_paged_kv_append(const pkv_cache_desc* cache, const void* k, const void* v,
+                               const int64_t* slot_mapping, int64_t num_tokens, pkv_stream_t stream) {
+  t_last_error.clear();
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens must be >= 0");
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping) return fail(PKV_ERR_INVALID_ARG, "k, v and slot_mapping must be non-NULL");
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(PKV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  if (!aligned(slot_mapping, 8)) return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  cudaError_t e = pkv::launch_append(k, v, slot_mapping, num_tokens, cache->num_kv_heads, cache->head_dim,
+                                     cache->kv_dtype == PKV_KV_FP8_E4M3, cache->k_cache, cache->v_cache,
+                                     cache->num_blocks * 16, cache->scales, dev->status,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PKV_OK;
+}
+
+int32_t pkv_decode_partition_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_context_len) {
+  t_last_error.clear();
+  if (batch <= 0 || num_kv_heads <= 0 || max_context_len < 0) {
+    fail(PKV_ERR_INVALID_ARG, "batch, num_kv_heads must be positive and max_context_len >= 0");
+    return 0;
+  }
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != PKV_OK) return 0;
+  return choose_split(batch, num_kv_heads, max_context_len, dev->sm_count).split_blocks * 16;
+}
+
+size_t pkv_decode_workspace_tickets_bytes(void) { return static_cast<size_t>(kTickets) * sizeof(int32_t); }
+
+static pkv_status plan(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_t max_len, bool fp8, Split* sp,
+                       WsLayout* ws, Variant* var, DeviceInfo** devp) {
+  if (batch < 0 || batch > 65535) return fail(PKV_ERR_INVALID_ARG, "batch must be in [0, 65535]");
+  if (hkv <= 0 || hq <= 0 || hq % hkv != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", hq, hkv);
+  const int g = hq / hkv;
+  if (g != 1 && g != 2 && g != 4 && g != 8)
+    return fail(PKV_ERR_UNSUPPORTED, "query-group size %d not in {1, 2, 4, 8}", g);
+  if (d != 64 && d != 128) return fail(PKV_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", d);
+  if (max_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len must be >= 0");
+  DeviceInfo* dev = nullptr;
+  pkv_status st = device_info(&dev);
+  if (st != PKV_OK) return st;
+  *var = pick_variant(d, fp8, g);
+  const pkv::DecodeLaunchInfo li = var->info();
+  *sp = fit_split(choose_split(batch, hkv, max_len, dev->sm_count), g, max_len, li.tile_area_bytes);
+  if (sp->max_splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "context too long for the partition grid");
+  *ws = ws_layout(batch, hkv, g, d, *sp);
+  *devp = dev;
+  return PKV_OK;
+}
+
+size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t max_context_len) {
+  t_last_error.clear();
+  Split sp;
+  WsLayout ws;
+  Variant var;
+  DeviceInfo* dev;
+  // the workspace does not depend on the element type of the pool
+  if (plan(batch, num_q_heads, num_kv_heads, head_dim, max_context_len, false, &sp, &ws, &var, &dev) != PKV_OK)
+    return 0;
+  return ws.total;
+}
+
+pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                                      int32_t num_q_heads, int32_t max_context_len, float softmax_scale, void* out,
+                                      pkv_out_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                      pkv_stream_t stream) {
+  t_last_error.clear();
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (batch == 0) return PKV_OK;
+  if (!q || !block_tables || !context_lens || !out)
+    return fail(PKV_ERR_INVALID_ARG, "q, block_tables, context_lens and out must be non-NULL");
+  if (!aligned(q, 16)) return fail(PKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (!aligned(out, 16)) return fail(PKV_ERR_INVALID_ARG, "out must be 16-byte aligned");
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return fail(PKV_ERR_INVALID_ARG, "block_tables and context_lens must be 4-byte aligned");
+  if (out_dtype != PKV_OUT_BF16 && out_dtype != PKV_OUT_FP32)
+    return fail(PKV_ERR_INVALID_ARG, "unknown out_dtype %d", static_cast<int>(out_dtype));
+  if (max_blocks_per_seq <= 0) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
+    return fail(PKV_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq * 16 = %lld", max_context_len,
+                static_cast<long long>(max_blocks_per_seq) * 16);
+  if (!std::isfinite(softmax_scale)) return fail(PKV_ERR_INVALID_ARG, "softmax_scale must be finite");
+  const bool fp8 = cache->kv_dtype == PKV_KV_FP8_E4M3;
+  Split sp;
+  WsLayout ws;
+  Variant var;
+  DeviceInfo* dev = nullptr;
+  st = plan(batch, num_q_heads, cache->num_kv_heads, cache->head_dim, max_context_len, fp8, &sp, &ws, &var, &dev);
+  if (st != PKV_OK) return st;
+  if (ws.total > 0) {
+    if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", ws.total);
+    if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (workspace_bytes < ws.total)
+      return fail(PKV_ERR_WORKSPACE, "workspace has %zu bytes, %zu required", workspace_bytes, ws.total);
+  }
+  CUtensorMap tk, tv;
+  if (!encode_kv_map(&tk, cache->k_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8) ||
+      !encode_kv_map(&tv, cache->v_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8))
+    return fail(PKV_ERR_INVALID_ARG, "cannot describe the KV pool as a TMA tensor map");
+
+  pkv::DecodeParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.scales = cache->scales;
+  p.out = out;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  p.tickets = ws.total ? reinterpret_cast<int32_t*>(wsb) : nullptr;
+  p.part_ml = ws.total ? reinterpret_cast<float*>(wsb + ws.tickets) : nullptr;
+  p.part_acc = ws.total ? reinterpret_cast<float*>(wsb + ws.tickets + ws.ml) : nullptr;
+  p.status = dev->status;
+  p.max_blocks = max_blocks_per_seq;
+  p.hq = num_q_heads;
+  p.hkv = cache->num_kv_heads;
+  p.num_blocks = static_cast<int>(cache->num_blocks);
+  p.max_context_len = max_context_len;
+  p.split_blocks = sp.split_blocks;
+  p.max_splits = sp.max_splits;
+  p.score_scale = softmax_scale * 1.4426950408889634f;  // log2(e)
+  p.out_fp32 = out_dtype == PKV_OUT_FP32;
+  int device = 0;
+  cudaGetDevice(&device);
+  const dim3 grid(static_cast<unsigned>(cache->num_kv_heads), static_cast<unsigned>(sp.max_splits),
+                  static_cast<unsigned>(batch));
+  cudaError_t e = var.launch(tk, tv, p, grid, reinterpret_cast<cudaStream_t>(stream), device);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return PKV_OK;
+}
+
+pkv_status pkv_check_device_status(pkv_stream_t stream, uint32_t* flags) {
+  t_last_error.clear();
+  DeviceInfo* dev = nullptr;
+  pkv_status st = device_info(&dev);
+  if (st != PKV_OK) return st;
+  uint32_t host = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&host, dev->status, sizeof host, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  if (flags) *flags = host;
+  if (host) {
+    e = cudaMemsetAsync(dev->status, 0, sizeof host, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device status word");
+    return fail(PKV_ERR_DEVICE_CHECK, "device-side check failed (flags 0x%x)", host);
+  }
+  return PKV_OK;
+}
+
+}  // extern "C"
