@@ -11,16 +11,21 @@
 //   * warp NWC (the producer) reads the block-table entries 32 at a time and issues one
 //     TMA tensor load per K tile and per V tile (16 tokens x head_dim of kv head h) into a
 //     ring of STAGES shared-memory stages, completing on per-stage mbarriers;
-//   * warps 0..NWC-1 (consumers) take the partition's blocks round-robin; each keeps its
-//     own online-softmax state for all G = Hq/Hkv query heads of the group, so every K/V
-//     element is widened to fp32 once and used by all G heads;
-//   * scores: lane l owns head_dim elements [l*D/32, (l+1)*D/32); per chunk of TC tokens it
-//     forms the G*TC partial dot products over its slice and sums them across the warp
-//     with a transposing butterfly (each level halves the values a lane holds), so a lane
-//     ends with one finished score; the registers are permuted per lane so that every
-//     level adds the same register half on every lane (no selects);
+//   * warps 0..NWC-1 (consumers) serve up to GW = min(G, 4) query heads each (a group of
+//     G = 8 heads is split over two warps that read the same tiles); the warps of one head
+//     group take the partition's blocks round-robin, each with its own online-softmax
+//     state, so every K/V element is widened to fp32 once per head group;
+//   * scores: lane l owns head_dim elements [l*D/32, (l+1)*D/32); per chunk of TC = 16/GW
+//     tokens it forms the 16 partial dot products (GW heads x TC tokens) over its slice and
+//     sums them across the warp with a transposing butterfly (each level halves the values
+//     a lane holds; the last level is a plain butterfly), so lanes 2k and 2k+1 end with the
+//     same finished score; the registers are permuted per lane so that every level adds the
+//     same register half on every lane (no selects);
 //   * P V: the weights go through a per-warp shared buffer; lane l accumulates its
-//     head_dim slice for all G heads with packed fp32x2 FMAs;
+//     head_dim slice for its heads with packed fp32x2 FMAs into (even token, odd token)
+//     accumulator pairs, so neither operand of a packed FMA needs duplicating; full blocks
+//     take a branch-free path, the one partial block of a sequence a masked one; the
+//     rescale by exp(m_old - m_new) runs only when a running max actually moved;
 //   * the consumer warps' states are merged in shared memory; a single-partition sequence
 //     writes its output directly, otherwise the partition's (m, l, unnormalised acc) go to
 //     the workspace and the last CTA of (b, h) to finish -- found with an atomic ticket, no
@@ -56,35 +61,38 @@ struct DecodeParams {
 
 template <int D, int G, bool FP8, int NWC, int STAGES>
 struct DecodeCfg {
-  static constexpr int kDPL = D / 32;                 // head_dim elements per lane
-  static constexpr int kTC = (G >= 2) ? 32 / G : 16;  // tokens per score chunk (G*TC values)
-  static constexpr int kN = G * kTC;                  // partial dot products per chunk (32, or 16 for G=1)
-  static constexpr int kLogN = (kN == 32) ? 5 : 4;
-  static constexpr int kNCH = kBlockSize / kTC;       // chunks per block
-  static constexpr int kLPG = 32 / G;                 // lanes holding scores of one query head
+  static constexpr int kGW = G < 4 ? G : 4;            // query heads per consumer warp
+  static constexpr int kHG = G / kGW;                  // head groups (warps sharing a tile)
+  static constexpr int kWPH = NWC / kHG;               // consumer warps per head group
+  static constexpr int kDPL = D / 32;                  // head_dim elements per lane
+  static constexpr int kTC = 16 / kGW;                 // tokens per score chunk
+  static constexpr int kNCH = kBlockSize / kTC;        // chunks per block (== kGW)
   static constexpr int kESZ = FP8 ? 1 : 2;
-  static constexpr int kTileBytes = kBlockSize * D * kESZ;
+  static constexpr int kRowBytes = D * kESZ;
+  static constexpr int kTileBytes = kBlockSize * kRowBytes;
   static constexpr int kThreads = (NWC + 1) * 32;
-  // shared memory: [STAGES] K tiles, [STAGES] V tiles, per-warp P (16 x G) + alpha (G),
-  // then mbarriers.  The end-of-CTA merge reuses the tile area.
-  static constexpr int kPBytes = NWC * (kBlockSize * G + G) * 4;
+  // per consumer warp: P[GW][16] weights and GW (alpha, alpha) pairs, rounded to 16 bytes
+  // so that every warp's P rows stay aligned for 16-byte shared loads
+  static constexpr int kPWarpFloats = (kGW * kBlockSize + 2 * kGW + 3) / 4 * 4;
+  static constexpr int kPBytes = NWC * kPWarpFloats * 4;
   static constexpr int kTilesBytes = 2 * STAGES * kTileBytes;
   static constexpr int kBarOffset = ((kTilesBytes + kPBytes) + 15) / 16 * 16;
   static constexpr int kSmemBytes = kBarOffset + 2 * STAGES * 8;
-  // merge scratch in the tile area: per warp m[G], l[G], acc[G][D]
-  static constexpr int kMergeBytes = NWC * (2 * G + G * D) * 4;
+  // merge scratch in the tile area: per warp m[GW], l[GW], acc[GW][D]
+  static constexpr int kMergeBytes = NWC * (2 * kGW + kGW * D) * 4;
   static_assert(kMergeBytes <= kTilesBytes, "merge scratch must fit in the tile ring");
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size");
+  static_assert(NWC % kHG == 0, "consumer warps per head group");
+  static_assert(kPWarpFloats % 4 == 0 && kTilesBytes % 16 == 0, "16-byte aligned P buffers");
 };
 
-// Load this lane's slice of row `row` of a K/V tile and widen it to fp32 (E4M3 values
-// come out times 2^-120; the factor is folded into q and into the output scale).
+// Widen kDPL consecutive elements at p (this lane's slice of one tile row) to fp32.
+// E4M3 values come out times 2^-120; the factor is folded into q and the output scale.
 template <int D, bool FP8>
-__device__ __forceinline__ void load_row(const uint8_t* tile, int row, int lane, float (&x)[D / 32]) {
+__device__ __forceinline__ void load_slice(const uint8_t* p, float (&x)[D / 32]) {
   constexpr int DPL = D / 32;
   if constexpr (!FP8) {
-    const uint8_t* p = tile + (row * D + lane * DPL) * 2;
     if constexpr (DPL == 4) {
       const uint2 w = *reinterpret_cast<const uint2*>(p);
       x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
@@ -93,7 +101,6 @@ __device__ __forceinline__ void load_row(const uint8_t* tile, int row, int lane,
       x[0] = bf16_lo(w); x[1] = bf16_hi(w);
     }
   } else {
-    const uint8_t* p = tile + row * D + lane * DPL;
     if constexpr (DPL == 4) {
       const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
       x[0] = e4m3_x2m120<0>(w); x[1] = e4m3_x2m120<1>(w); x[2] = e4m3_x2m120<2>(w); x[3] = e4m3_x2m120<3>(w);
@@ -104,12 +111,143 @@ __device__ __forceinline__ void load_row(const uint8_t* tile, int row, int lane,
   }
 }
 
+// Online-softmax state of one consumer warp for its GW query heads.
+template <int D, int GW>
+struct WarpState {
+  float2 acc[GW][D / 32];  // (even-token, odd-token) partial sums of P V, this lane's slice
+  float m;                 // running max (log2 units) of head sig_g
+  float l;                 // this lane's share of the running sum of head sig_g
+};
+
+// One 16-token block: scores, online-softmax update, P V.  `valid` tokens (1..16) count.
+template <int D, int GW, bool FP8, bool FULL>
+__device__ __forceinline__ void consume_block(const uint8_t* kt, const uint8_t* vt, int valid, float smul,
+                                              const float2 (&qd)[GW][D / 32], const int (&rowoff)[16 / GW],
+                                              int sig_g, int sig_t, int lane, float* pbuf, float2* abuf,
+                                              WarpState<D, GW>& st) {
+  constexpr int DPL = D / 32, TC = 16 / GW, NCH = kBlockSize / TC;
+  constexpr int ROW = D * (FP8 ? 1 : 2);
+  const int slice = lane * DPL * (FP8 ? 1 : 2);
+
+  // ---- scores: one finished score per lane pair per chunk
+  float sc[NCH];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    float kx[TC][DPL];
+#pragma unroll
+    for (int ts = 0; ts < TC; ++ts) load_slice<D, FP8>(kt + c * TC * ROW + rowoff[ts], kx[ts]);
+    float part[16];
+#pragma unroll
+    for (int gs = 0; gs < GW; ++gs)
+#pragma unroll
+      for (int tp = 0; tp < TC; tp += 2) {
+        float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) a = ffma2(qd[gs][i], make_float2(kx[tp][i], kx[tp + 1][i]), a);
+        part[gs * TC + tp] = a.x;
+        part[gs * TC + tp + 1] = a.y;
+      }
+    // transposing butterfly over 16 values: lane bit 4..1 select the half kept at each level
+    {
+      float r[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) r[i] = shfl_xor(part[i + 8], 16);
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        const float2 s2 = fadd2(make_float2(part[i], part[i + 1]), make_float2(r[i], r[i + 1]));
+        part[i] = s2.x; part[i + 1] = s2.y;
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) r[i] = shfl_xor(part[i + 4], 8);
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        const float2 s2 = fadd2(make_float2(part[i], part[i + 1]), make_float2(r[i], r[i + 1]));
+        part[i] = s2.x; part[i + 1] = s2.y;
+      }
+      r[0] = shfl_xor(part[2], 4);
+      r[1] = shfl_xor(part[3], 4);
+      {
+        const float2 s2 = fadd2(make_float2(part[0], part[1]), make_float2(r[0], r[1]));
+        part[0] = s2.x; part[1] = s2.y;
+      }
+      part[0] += shfl_xor(part[1], 2);
+      part[0] += shfl_xor(part[0], 1);
+    }
+    if constexpr (FULL) {
+      sc[c] = part[0] * smul;
+    } else {
+      sc[c] = (c * TC + sig_t) < valid ? part[0] * smul : -INFINITY;
+    }
+  }
+
+  // ---- online softmax for head sig_g (lanes 2k, 2k+1 hold the same scores)
+  float bmax = sc[0];
+#pragma unroll
+  for (int c = 1; c < NCH; ++c) bmax = fmaxf(bmax, sc[c]);
+#pragma unroll
+  for (int m = 2; m <= TC; m <<= 1) bmax = fmaxf(bmax, shfl_xor(bmax, m));
+  const bool moved = __any_sync(kFull, bmax > st.m);
+  if (moved) {
+    const float m_new = fmaxf(st.m, bmax);
+    const float alpha = (m_new == st.m) ? 1.0f : fast_exp2(st.m - m_new);
+    st.l *= alpha;
+    st.m = m_new;
+    if ((lane & (2 * TC - 1)) == 0) abuf[sig_g] = make_float2(alpha, alpha);
+  }
+  float psum = 0.f;
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    const float pv = fast_exp2(sc[c] - st.m);
+    psum += pv;
+    pbuf[sig_g * kBlockSize + c * TC + sig_t] = pv;
+  }
+  st.l += psum;
+  __syncwarp();
+  if (moved) {
+#pragma unroll
+    for (int g = 0; g < GW; ++g) {
+      const float2 a2 = abuf[g];
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) st.acc[g][i] = fmul2(st.acc[g][i], a2);
+    }
+  }
+
+  // ---- P V over this lane's head_dim slice, tokens in (even, odd) pairs
+#pragma unroll
+  for (int t4 = 0; t4 < kBlockSize; t4 += 4) {
+    float4 pq[GW];
+#pragma unroll
+    for (int g = 0; g < GW; ++g) pq[g] = *reinterpret_cast<const float4*>(pbuf + g * kBlockSize + t4);
+#pragma unroll
+    for (int pr = 0; pr < 2; ++pr) {
+      const int t0 = t4 + 2 * pr;
+      float v0[DPL], v1[DPL];
+      load_slice<D, FP8>(vt + t0 * ROW + slice, v0);
+      load_slice<D, FP8>(vt + (t0 + 1) * ROW + slice, v1);
+      if constexpr (!FULL) {
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) {  // rows past the sequence may hold anything (even NaN)
+          v0[i] = t0 < valid ? v0[i] : 0.f;
+          v1[i] = t0 + 1 < valid ? v1[i] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < GW; ++g) {
+        const float2 pp = pr == 0 ? make_float2(pq[g].x, pq[g].y) : make_float2(pq[g].z, pq[g].w);
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) st.acc[g][i] = ffma2(pp, make_float2(v0[i], v1[i]), st.acc[g][i]);
+      }
+    }
+  }
+  __syncwarp();  // the next block rewrites pbuf
+}
+
 template <int D, int G, bool FP8, int NWC, int STAGES>
 __global__ void __launch_bounds__((NWC + 1) * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeParams p) {
   using C = DecodeCfg<D, G, FP8, NWC, STAGES>;
-  constexpr int DPL = C::kDPL, TC = C::kTC, N = C::kN, NCH = C::kNCH, LPG = C::kLPG;
+  constexpr int DPL = C::kDPL, TC = C::kTC, GW = C::kGW, HG = C::kHG, WPH = C::kWPH;
 
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* k_tiles = smem;
@@ -156,7 +294,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+      mbar_init(&empty_bar[i], HG);  // every head group's warp releases the stage
     }
     fence_mbar_init();
   }
@@ -166,8 +304,8 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   // (q * 2^64 keeps every product a normal number, the rest goes into the score scale).
   float qmul = p.score_scale, smul = 1.0f;
   if constexpr (FP8) {
-    qmul = 18446744073709551616.0f;                               // 2^64
-    smul = p.score_scale * p.scales[h] * 72057594037927936.0f;    // * 2^56
+    qmul = 18446744073709551616.0f;                             // 2^64
+    smul = p.score_scale * p.scales[h] * 72057594037927936.0f;  // * 2^56
   }
 
   bool timed_out = false;
@@ -214,28 +352,32 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
     __syncwarp();
   }
 
-  // consumer state (the producer warp keeps the neutral values)
-  const int sigma = lane >> (5 - C::kLogN);  // value index this lane ends up holding
-  const int sig_g = sigma / TC;               // == this lane's query head within the group
-  const int sig_t = sigma % TC;               // == this lane's token within a chunk
-  float m_run = -INFINITY;                    // running max (log2 units) of head sig_g
-  float l_run = 0.f;                          // this lane's share of the running sum
-  float2 acc[G][DPL / 2];
+  // consumer lane roles: after the butterfly lanes 2k, 2k+1 hold head sig_g, token sig_t
+  const int hg = warp % HG;                 // head group of this warp
+  const int sigma = lane >> 1;
+  const int sig_g = sigma / TC;
+  const int sig_t = sigma % TC;
+  WarpState<D, GW> st;
+  st.m = -INFINITY;
+  st.l = 0.f;
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+  for (int g = 0; g < GW; ++g)
 #pragma unroll
-    for (int i = 0; i < DPL / 2; ++i) acc[g][i] = make_float2(0.f, 0.f);
+    for (int i = 0; i < DPL; ++i) st.acc[g][i] = make_float2(0.f, 0.f);
 
   if (warp < NWC) {
     // ================================================================ consumer warps
-    float* pbuf = p_all + warp * (kBlockSize * G + G);  // P[t][g], then alpha[g]
-    float* abuf = pbuf + kBlockSize * G;
-    // q slice, permuted: register slot gs holds query head gs ^ sig_g (see header)
-    float2 qd[G][DPL];
-    {
-      const uint16_t* qrow = p.q + (static_cast<size_t>(b) * p.hq + hq0) * D + lane * DPL;
+    float* pbuf = p_all + warp * C::kPWarpFloats;  // P[g][t]
+    float2* abuf = reinterpret_cast<float2*>(pbuf + GW * kBlockSize);
+    int rowoff[TC];
 #pragma unroll
-      for (int gs = 0; gs < G; ++gs) {
+    for (int ts = 0; ts < TC; ++ts) rowoff[ts] = (ts ^ sig_t) * C::kRowBytes + lane * DPL * C::kESZ;
+    // q slice of the warp's heads, permuted: slot gs holds head hg*GW + (gs ^ sig_g), as (q, q)
+    float2 qd[GW][DPL];
+    {
+      const uint16_t* qrow = p.q + (static_cast<size_t>(b) * p.hq + hq0 + hg * GW) * D + lane * DPL;
+#pragma unroll
+      for (int gs = 0; gs < GW; ++gs) {
         const uint16_t* qq = qrow + static_cast<size_t>(gs ^ sig_g) * D;
         float x[DPL];
         if constexpr (DPL == 4) {
@@ -250,150 +392,62 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       }
     }
 
-    for (int it = warp; it < nloc; it += NWC) {
-      const int st = it % STAGES;
-      if (!mbar_wait(&full_bar[st], (it / STAGES) & 1)) {
+    for (int it = warp / HG; it < nloc; it += WPH) {
+      const int sg = it % STAGES;
+      if (!mbar_wait(&full_bar[sg], (it / STAGES) & 1)) {
         if (lane == 0) set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
         timed_out = true;
         break;
       }
-      const uint8_t* kt = k_tiles + st * C::kTileBytes;
-      const uint8_t* vt = v_tiles + st * C::kTileBytes;
+      const uint8_t* kt = k_tiles + sg * C::kTileBytes;
+      const uint8_t* vt = v_tiles + sg * C::kTileBytes;
       const int valid = min(kBlockSize, len - (blk0 + it) * kBlockSize);  // >= 1
-
-      // ---- scores: one finished score per lane per chunk
-      float sc[NCH];
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        float kx[TC][DPL];
-#pragma unroll
-        for (int ts = 0; ts < TC; ++ts) load_row<D, FP8>(kt, c * TC + (ts ^ sig_t), lane, kx[ts]);
-        float part[N];
-        static_assert(TC % 2 == 0, "token pairs");
-#pragma unroll
-        for (int gs = 0; gs < G; ++gs)
-#pragma unroll
-          for (int tp = 0; tp < TC; tp += 2) {
-            float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int i = 0; i < DPL; ++i) a = ffma2(qd[gs][i], make_float2(kx[tp][i], kx[tp + 1][i]), a);
-            part[gs * TC + tp] = a.x;
-            part[gs * TC + tp + 1] = a.y;
-          }
-        // transposing butterfly: after level j a lane holds half as many partial sums
-        int n = N;
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-          if (n >= 2) {
-            const int half = n >> 1;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (i < half) part[i] += shfl_xor(part[i + half], m);
-            n = half;
-          } else {
-            part[0] += shfl_xor(part[0], m);
-          }
-        }
-        const bool ok = (c * TC + sig_t) < valid;
-        sc[c] = ok ? part[0] * smul : -INFINITY;
-      }
-
-      // ---- online softmax for head sig_g (all lanes of the head agree on the max)
-      float bmax = sc[0];
-#pragma unroll
-      for (int c = 1; c < NCH; ++c) bmax = fmaxf(bmax, sc[c]);
-#pragma unroll
-      for (int m = 1; m < LPG; m <<= 1) bmax = fmaxf(bmax, shfl_xor(bmax, m));
-      const float m_new = fmaxf(m_run, bmax);
-      const float alpha = fast_exp2(m_run - m_new);
-      float psum = 0.f;
-#pragma unroll
-      for (int c = 0; c < NCH; ++c) {
-        const float pv = fast_exp2(sc[c] - m_new);
-        psum += pv;
-        pbuf[(c * TC + sig_t) * G + sig_g] = pv;
-      }
-      l_run = l_run * alpha + psum;
-      m_run = m_new;
-      if ((lane & (LPG - 1)) == 0) abuf[sig_g] = alpha;
-      __syncwarp();
-
-      // ---- rescale and accumulate P V over this lane's head_dim slice
-      {
-        float al[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) al[g] = abuf[g];
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int i = 0; i < DPL / 2; ++i) acc[g][i] = fmul2(acc[g][i], make_float2(al[g], al[g]));
-      }
-#pragma unroll
-      for (int t = 0; t < kBlockSize; ++t) {
-        if (t < valid) {
-          float vx[DPL];
-          load_row<D, FP8>(vt, t, lane, vx);
-          float pw[G];
-          if constexpr (G >= 4) {
-#pragma unroll
-            for (int g4 = 0; g4 < G; g4 += 4) {
-              const float4 f = *reinterpret_cast<const float4*>(pbuf + t * G + g4);
-              pw[g4] = f.x; pw[g4 + 1] = f.y; pw[g4 + 2] = f.z; pw[g4 + 3] = f.w;
-            }
-          } else {
-#pragma unroll
-            for (int g = 0; g < G; ++g) pw[g] = pbuf[t * G + g];
-          }
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int i = 0; i < DPL / 2; ++i)
-              acc[g][i] = ffma2(make_float2(pw[g], pw[g]), make_float2(vx[2 * i], vx[2 * i + 1]), acc[g][i]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
+      if (valid == kBlockSize)
+        consume_block<D, GW, FP8, true>(kt, vt, valid, smul, qd, rowoff, sig_g, sig_t, lane, pbuf, abuf, st);
+      else
+        consume_block<D, GW, FP8, false>(kt, vt, valid, smul, qd, rowoff, sig_g, sig_t, lane, pbuf, abuf, st);
+      if (lane == 0) mbar_arrive(&empty_bar[sg]);
     }
   }
 
   // ================================================================ merge the consumer warps
   __syncthreads();  // ring drained (every issued copy landed and was consumed)
-  float* mw = reinterpret_cast<float*>(smem);  // [NWC][G] max
-  float* lw = mw + NWC * G;                    // [NWC][G] sum
-  float* aw = lw + NWC * G;                    // [NWC][G][D] unnormalised output
+  float* mw = reinterpret_cast<float*>(smem);  // [NWC][GW] max
+  float* lw = mw + NWC * GW;                   // [NWC][GW] sum
+  float* aw = lw + NWC * GW;                   // [NWC][GW][D] unnormalised output
   if (warp < NWC) {
-    float lsum = l_run;
+    float lsum = st.l;
 #pragma unroll
-    for (int m = 1; m < LPG; m <<= 1) lsum += shfl_xor(lsum, m);
-    if (G == 1) lsum *= 0.5f;  // with G == 1 every score is held by two lanes
-    if ((lane & (LPG - 1)) == 0) {
-      mw[warp * G + sig_g] = m_run;
-      lw[warp * G + sig_g] = lsum;
+    for (int m = 2; m <= TC; m <<= 1) lsum += shfl_xor(lsum, m);  // lane 2k+1 duplicates 2k
+    if ((lane & (2 * TC - 1)) == 0) {
+      mw[warp * GW + sig_g] = st.m;
+      lw[warp * GW + sig_g] = lsum;
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int g = 0; g < GW; ++g)
 #pragma unroll
-      for (int i = 0; i < DPL / 2; ++i)
-        *reinterpret_cast<float2*>(aw + (warp * G + g) * D + lane * DPL + 2 * i) = acc[g][i];
+      for (int i = 0; i < DPL; ++i) aw[(warp * GW + g) * D + lane * DPL + i] = st.acc[g][i].x + st.acc[g][i].y;
   }
   __syncthreads();
 
-  // per query head: max over warps, weights 2^(m_w - M); then each element
+  // per query head: max over the head group's warps, weights 2^(m_w - M); then each element
   const size_t out_row0 = static_cast<size_t>(b) * p.hq + hq0;
   float vfix = 1.0f;  // E4M3 values carry 2^-120; V's scale and that factor go to the output
   if constexpr (FP8) vfix = p.scales[p.hkv + h];
   const bool single = (nsplit == 1);
   for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
     const int g = e / D, d = e % D;
+    const int ghg = g / GW, gw = g % GW;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NWC; ++w) M = fmaxf(M, mw[w * G + g]);
+    for (int k = 0; k < WPH; ++k) M = fmaxf(M, mw[(ghg + HG * k) * GW + gw]);
     float num = 0.f, den = 0.f;
 #pragma unroll
-    for (int w = 0; w < NWC; ++w) {
-      const float wt = fast_exp2(mw[w * G + g] - M);  // empty warps: 2^-inf = 0
-      num = fmaf(wt, aw[(w * G + g) * D + d], num);
-      den = fmaf(wt, lw[w * G + g], den);
+    for (int k = 0; k < WPH; ++k) {
+      const int w = ghg + HG * k;
+      const float wt = fast_exp2(mw[w * GW + gw] - M);  // warps without blocks: 2^-inf = 0
+      num = fmaf(wt, aw[(w * GW + gw) * D + d], num);
+      den = fmaf(wt, lw[w * GW + gw], den);
     }
     if (single) {
       float o = num / den;
