@@ -54,7 +54,7 @@ struct DecodeParams {
   int num_blocks;       // pool size in blocks
   int max_context_len;  // launch bound on context_lens
   int split_blocks;     // blocks per partition
-  int max_splits;       // gridDim.y
+  int max_splits;       // gridDim.z
   float score_scale;    // softmax_scale * log2(e)
   int out_fp32;
 };
@@ -84,6 +84,10 @@ struct DecodeCfg {
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(G == 1 || G == 2 || G == 4 || G == 8, "group size");
   static_assert(NWC % kHG == 0, "consumer warps per head group");
+  // Each stage must always be consumed by the same warps: a warp then waits on a stage
+  // barrier only after consuming that stage's previous phase itself, so a phase parity can
+  // never be mistaken for the one two phases back.
+  static_assert(STAGES % kWPH == 0, "ring depth must be a multiple of the warps per head group");
   static_assert(kPWarpFloats % 4 == 0 && kTilesBytes % 16 == 0, "16-byte aligned P buffers");
 };
 
@@ -256,9 +260,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
   uint64_t* empty_bar = full_bar + STAGES;
 
+  // grid (kv head, sequence, partition): the block scheduler hands out every sequence's first
+  // partition before any second one, so the long sequences' last partitions come last
   const int h = blockIdx.x;
-  const int s = blockIdx.y;
-  const int b = blockIdx.z;
+  const int b = blockIdx.y;
+  const int s = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -291,6 +297,23 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   const int blk0 = s * p.split_blocks;
   const int nloc = min(nblk, blk0 + p.split_blocks) - blk0;
 
+  // issue the first global loads now, so their latency overlaps the barrier set-up
+  const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk0;
+  int ids = (warp == NWC && lane < nloc) ? row[lane] : 0;
+  const int hg = warp % HG;  // head group of a consumer warp
+  uint32_t qbits[GW][DPL / 2];
+  if (warp < NWC) {
+    const int sig_g0 = (lane >> 1) / TC;
+    const uint16_t* qrow = p.q + (static_cast<size_t>(b) * p.hq + hq0 + hg * GW) * D + lane * DPL;
+#pragma unroll
+    for (int gs = 0; gs < GW; ++gs) {
+      const uint32_t* qq = reinterpret_cast<const uint32_t*>(qrow + static_cast<size_t>(gs ^ sig_g0) * D);
+#pragma unroll
+      for (int i = 0; i < DPL / 2; ++i) qbits[gs][i] = qq[i];
+    }
+  }
+  if (threadIdx.x == NWC * 32) tma_prefetch_desc(&tm_k), tma_prefetch_desc(&tm_v);
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&full_bar[i], 1);
@@ -312,8 +335,6 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
 
   if (warp == NWC) {
     // ================================================================ producer warp
-    const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk0;
-    int ids = (lane < nloc) ? row[lane] : 0;
     int issued = 0;
     for (int base = 0; base < nloc && !timed_out; base += 32) {
       const int next = (base + 32 + lane < nloc) ? row[base + 32 + lane] : 0;  // prefetch
@@ -353,7 +374,6 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   }
 
   // consumer lane roles: after the butterfly lanes 2k, 2k+1 hold head sig_g, token sig_t
-  const int hg = warp % HG;                 // head group of this warp
   const int sigma = lane >> 1;
   const int sig_g = sigma / TC;
   const int sig_t = sigma % TC;
@@ -374,23 +394,14 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
     for (int ts = 0; ts < TC; ++ts) rowoff[ts] = (ts ^ sig_t) * C::kRowBytes + lane * DPL * C::kESZ;
     // q slice of the warp's heads, permuted: slot gs holds head hg*GW + (gs ^ sig_g), as (q, q)
     float2 qd[GW][DPL];
-    {
-      const uint16_t* qrow = p.q + (static_cast<size_t>(b) * p.hq + hq0 + hg * GW) * D + lane * DPL;
 #pragma unroll
-      for (int gs = 0; gs < GW; ++gs) {
-        const uint16_t* qq = qrow + static_cast<size_t>(gs ^ sig_g) * D;
-        float x[DPL];
-        if constexpr (DPL == 4) {
-          const uint2 w = *reinterpret_cast<const uint2*>(qq);
-          x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-        } else {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(qq);
-          x[0] = bf16_lo(w); x[1] = bf16_hi(w);
-        }
+    for (int gs = 0; gs < GW; ++gs)
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) qd[gs][i] = make_float2(x[i] * qmul, x[i] * qmul);
+      for (int i = 0; i < DPL / 2; ++i) {
+        const float lo = bf16_lo(qbits[gs][i]) * qmul, hi = bf16_hi(qbits[gs][i]) * qmul;
+        qd[gs][2 * i] = make_float2(lo, lo);
+        qd[gs][2 * i + 1] = make_float2(hi, hi);
       }
-    }
 
     for (int it = warp / HG; it < nloc; it += WPH) {
       const int sg = it % STAGES;

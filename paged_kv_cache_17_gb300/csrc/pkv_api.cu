@@ -19,7 +19,8 @@ namespace {
 
 constexpr int kVersion = 100;  // 0.1.0
 constexpr int kMaxDevices = 64;
-constexpr int kMinSplitBlocks = 16;  // a context partition covers at least 256 tokens
+constexpr int kMinSplitBlocks = 32;   // a context partition covers at least 512 tokens ...
+constexpr int kMaxSplitBlocks = 128;  // ... and at most 2048 (unless forced)
 // The workspace starts with a ticket region of fixed size, so a workspace reused for other
 // sizes never finds partial results of an earlier call where tickets are expected.  Launches
 // with more (sequence, kv head) units than tickets do not split the context: they already
@@ -118,9 +119,11 @@ struct Split {
   int max_splits;
 };
 
-// Partitions of equal logical length (a multiple of 16 tokens) so that a batch at its
-// maximal length spreads over about four CTAs per SM slot; never shorter than 256 tokens.
-// PKV_SPLIT_TOKENS (a positive multiple of 16) overrides the choice, for tuning and tests.
+// Partitions of equal logical length (a multiple of 16 tokens), sized so that a batch at its
+// maximal length spreads over about four waves of CTAs (three resident per SM), clamped to
+// 512..2048 tokens: shorter partitions cost more merging and CTA start-up, longer ones leave
+// a long tail of lone CTAs.  PKV_SPLIT_TOKENS (a positive multiple of 16) overrides the
+// choice, for tuning and tests.
 Split choose_split(int batch, int hkv, int max_context_len, int sm_count) {
   const int max_nblk = (max_context_len + 15) / 16;
   Split r{1, 1};
@@ -136,12 +139,11 @@ Split choose_split(int batch, int hkv, int max_context_len, int sm_count) {
   }
   if (sb == 0) {
     const long long units = static_cast<long long>(batch) * hkv;
-    const long long target = 4LL * sm_count * 2;  // ~two resident CTAs per SM, four waves
-    long long splits = (target + units - 1) / units;
-    if (splits < 1) splits = 1;
-    sb = static_cast<int>((max_nblk + splits - 1) / splits);
-    if (sb < kMinSplitBlocks) sb = kMinSplitBlocks;
-    sb = (sb + 3) / 4 * 4;
+    const long long slots = 4LL * sm_count * 3;
+    long long want = (static_cast<long long>(max_nblk) * units + slots - 1) / slots;
+    if (want < kMinSplitBlocks) want = kMinSplitBlocks;
+    if (want > kMaxSplitBlocks) want = kMaxSplitBlocks;
+    sb = static_cast<int>((want + 3) / 4 * 4);
   }
   if (sb > max_nblk) sb = max_nblk;
   r.split_blocks = sb;
@@ -367,8 +369,8 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q
   p.out_fp32 = out_dtype == PKV_OUT_FP32;
   int device = 0;
   cudaGetDevice(&device);
-  const dim3 grid(static_cast<unsigned>(cache->num_kv_heads), static_cast<unsigned>(sp.max_splits),
-                  static_cast<unsigned>(batch));
+  const dim3 grid(static_cast<unsigned>(cache->num_kv_heads), static_cast<unsigned>(batch),
+                  static_cast<unsigned>(sp.max_splits));
   cudaError_t e = var.launch(tk, tv, p, grid, reinterpret_cast<cudaStream_t>(stream), device);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
