@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clock-fill", action="store_true",
+                    help="do not run the untimed clock-sampling loop when the timed region is too short "
+                         "(for profiler runs)")
     return ap.parse_args()
 
 
@@ -276,7 +279,7 @@ def run_ours(args):
             torch.distributed.barrier()
         wall = time.perf_counter() - wall0
     clocks = clk.summary()
-    if clocks.get("samples", 0) < 3:
+    if clocks.get("samples", 0) < 3 and not args.no_clock_fill:
         # the timed region was shorter than the sampler's period: sample the same step loop
         # for another half second (untimed) and say so
         mid = torch.cuda.Event(enable_timing=True)  # keep the timed events untouched
