@@ -169,6 +169,30 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q
                                       pkv_stream_t stream);
 
 /*
+ * Decode attention without a caller-provided workspace.  (The pages describe no such
+ * call; it serves callers that cannot allocate device memory when they run a decode step:
+ * an allocator that has reserved all device memory for itself, a serving loop that
+ * forbids allocation after start-up, or a C caller with no allocator at hand.)
+ *   Arguments, results and errors are those of pkv_paged_decode_attention; the workspace
+ *   is a fixed 32 MiB array inside the library, one per device that loads it.
+ *   Calls whose workspace would exceed 32 MiB (pkv_decode_workspace_size) are rejected with
+ *   PKV_ERR_WORKSPACE before anything is enqueued.
+ *   The first call on a device looks up that device's copy of the array (with the device
+ *   current); make that first call before any stream capture.
+ *   All calls on a device share the one array and it keeps what the last call left; each
+ *   call clears the part that must start at zero.  Two calls whose work can overlap on
+ *   the GPU (different streams, or other devices' calls on this device) race on it.
+ *   It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ */
+pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const void* q,
+                                              const int32_t* block_tables,
+                                              int32_t max_blocks_per_seq,
+                                              const int32_t* context_lens, int32_t batch,
+                                              int32_t num_q_heads, int32_t max_context_len,
+                                              float softmax_scale, void* out,
+                                              pkv_out_dtype out_dtype, pkv_stream_t stream);
+
+/*
  * Read and clear the device status word of the current device after the work queued on
  * `stream` so far has finished (this call synchronises `stream`).  *flags receives the
  * PKV_DEVFLAG_* bits (may be NULL).  Returns PKV_ERR_DEVICE_CHECK if any bit was set,

@@ -43,7 +43,7 @@ DEVFLAG_WAIT_TIMEOUT = 0x8
 EXPORTED_SYMBOLS = (
     "pkv_paged_kv_append", "pkv_decode_workspace_size", "pkv_decode_workspace_tickets_bytes",
     "pkv_decode_partition_tokens", "pkv_paged_decode_attention", "pkv_check_device_status",
-    "pkv_status_string", "pkv_last_error", "pkv_version",
+    "pkv_status_string", "pkv_last_error", "pkv_version", "pkv_paged_decode_attention_noalloc",
 )
 
 
@@ -75,6 +75,9 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_decode_attention.restype = ctypes.c_int
     lib.pkv_paged_decode_attention.argtypes = [ctypes.POINTER(CacheDesc), P, P, i32, P, i32, i32, i32,
                                                ctypes.c_float, P, ctypes.c_int, P, sz, P]
+    lib.pkv_paged_decode_attention_noalloc.restype = ctypes.c_int
+    lib.pkv_paged_decode_attention_noalloc.argtypes = [ctypes.POINTER(CacheDesc), P, P, i32, P, i32, i32, i32,
+                                                       ctypes.c_float, P, ctypes.c_int, P]
     lib.pkv_check_device_status.restype = ctypes.c_int
     lib.pkv_check_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.pkv_status_string.restype = ctypes.c_char_p

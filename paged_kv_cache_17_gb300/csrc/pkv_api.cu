@@ -237,6 +237,8 @@ const char* pkv_status_string(pkv_status s) {
 
 const char* pkv_last_error(void) { return t_last_error.c_str(); }
 
+__attribute__((visibility("hidden"))) void pkv_internal_set_error(const char* msg) { t_last_error = msg; }
+
 int32_t pkv_version(void) { return kVersion; }
 
 pkv_status pkv_paged_kv_append(const pkv_cache_desc* cache, const void* k, const void* v,
