@@ -46,6 +46,12 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="llama3_8b", choices=W.ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="step", choices=["step", "copy_blocks"],
+                    help="step: append + decode attention (the headline); copy_blocks: the copy-on-write "
+                         "block copy alone")
+    ap.add_argument("--layout", default="shuffled", choices=["shuffled", "contiguous"],
+                    help="physical block order of the pool (contiguous = each sequence's blocks in order)")
+    ap.add_argument("--copy-pairs", type=int, default=4096, help="(src, dst) pairs per copy_blocks launch")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -235,7 +241,7 @@ def run_ours(args):
         torch.distributed.init_process_group("nccl", init_method="env://")
     dev = torch.device("cuda", torch.cuda.current_device())
     cfg = W.get(args.config)
-    w = W.make_workload(cfg, seed=cfg.seed + 1000 * rank)
+    w = W.make_workload(cfg, seed=cfg.seed + 1000 * rank, layout=args.layout)
     nb = step_bytes(w)
     B, hq, hkv, d = w.batch, cfg.hq, cfg.hkv, cfg.d
     max_len = int(w.context_lens.max())
@@ -365,12 +371,13 @@ def run_ours(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.kv_dtype == "bf16" else "e4m3",
-        "data": "synthetic (seeded N(0,1) bf16 q/K/V, shuffled 16-token block pool)",
+        "data": f"synthetic (seeded N(0,1) bf16 q/K/V, {args.layout} 16-token block pool)",
         "config": {"workload": f"{cfg.name}: batch {B}, context {cfg.len_range if cfg.kind == 'uniform' else 'mixed'}, "
                                f"Hq {hq}, Hkv {hkv}, D {d}, block 16, {cfg.kv_dtype} KV, append {w.slot_mapping.numel()} tokens",
                    "batch": B, "num_q_heads": hq, "num_kv_heads": hkv, "head_dim": d, "kv_dtype": cfg.kv_dtype,
                    "max_context_len": max_len, "total_context_tokens": w.total_tokens(),
                    "partition_tokens": pkv.partition_tokens(B, hkv, max_len),
+                   "layout": args.layout,
                    "l2": "flushed between timed steps (256 MiB write, untimed)", "parallelism": f"replicas x{ws}"},
         "us_per_step": round(ms_per_step * 1e3, 2),
         "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
@@ -385,6 +392,125 @@ def run_ours(args):
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "wall_s": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ copy-on-write block copy
+
+def copy_pairs(num_blocks: int, n: int, seed: int) -> torch.Tensor:
+    """n (src, dst) pairs over disjoint random blocks (no dst is also a src)."""
+    n = min(n, num_blocks // 2)
+    perm = torch.randperm(num_blocks, generator=torch.Generator().manual_seed(seed))
+    return torch.stack([perm[:n], perm[n:2 * n]], dim=1).contiguous()
+
+
+def oracle_copy_sample(w: W.Workload, pairs: torch.Tensor, budget_s: float):
+    """Time the oracle's block copy (one host thread) on the same pool and pairs."""
+    import oracle
+
+    a = w.np()
+    kc, vc = a["k_cache"], a["v_cache"]
+    pr = pairs.numpy()
+    moved = 2 * 2 * pr.shape[0] * kc[0].nbytes  # K and V, read + write
+    reps, dt = 0, 0.0
+    while dt < budget_s:
+        t0 = time.perf_counter()
+        oracle.copy_blocks(kc, vc, pr)
+        dt += time.perf_counter() - t0
+        reps += 1
+    return moved * reps / dt / 1e9, dt, reps
+
+
+def run_copy_blocks(args):
+    import paged_kv_cache_17_gb300 as pkv
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    cfg = W.get(args.config)
+    w = W.make_workload(cfg, seed=cfg.seed + 1000 * rank, layout=args.layout)
+    pairs_h = copy_pairs(w.num_blocks, args.copy_pairs, cfg.seed + 77 + 1000 * rank)
+    n = pairs_h.shape[0]
+    block_bytes = 16 * cfg.hkv * cfg.d * cfg.elem_bytes
+    moved = 2 * 2 * n * block_bytes  # K and V blocks, each read once and written once
+    kc, vc = w.k_cache.to(dev), w.v_cache.to(dev)
+    sc = None if w.scales is None else w.scales.to(dev)
+    pairs = pairs_h.to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        pkv.copy_blocks(pairs, kc, vc, scales=sc)
+    torch.cuda.synchronize()
+    assert pkv.check_device_status() == 0
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(dev.index) as clk:
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            pkv.copy_blocks(pairs, kc, vc, scales=sc)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+    clocks = clk.summary()
+    clocks["window"] = "timed region"
+    tot_ms = sum(a.elapsed_time(b) for a, b in evs)
+    if ws > 1:
+        tt = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        tot_ms = float(tt.item())
+    assert pkv.check_device_status() == 0
+    achieved = moved * args.steps / (tot_ms * 1e-3) / 1e9
+    # end to end: the pair list comes from pinned host memory every step
+    host_pairs = pairs_h.pin_memory()
+    dev_pairs = torch.empty_like(pairs)
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ee[i][0].record(stream)
+        dev_pairs.copy_(host_pairs, non_blocking=True)
+        pkv.copy_blocks(dev_pairs, kc, vc, scales=sc)
+        ee[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        gbs, dt, reps = oracle_copy_sample(w, pairs_h, min(args.cpu_seconds, 5.0))
+        cpu = {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"the same {n} pairs x {reps} passes (memcpy per block, one thread)",
+               "seconds": round(dt, 2)}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or FALLBACK_HBM_GBS
+    line = {
+        "metric": "copy-on-write block copy achieved HBM GB/s (bytes read + written)", "value": round(achieved * ws, 2),
+        "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8" if cfg.kv_dtype == "e4m3" else "bf16 (bit copy)",
+        "data": f"synthetic (seeded pool of {args.config}, {n} disjoint random block pairs)",
+        "config": {"workload": f"copy {n} blocks of {block_bytes} B (K and V) in the {args.config} pool "
+                               f"({w.num_blocks} blocks)", "pairs": n, "block_bytes": block_bytes,
+                   "l2": "flushed between timed launches (256 MiB write, untimed)", "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "copy_blocks_kernel",
+                     "peak_source": f"{peak_src} hbm_gbs (copy)"},
+        "e2e": {"value": round(moved * ws * args.steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(n * 16), "d2h_bytes_per_step": 0},
+        "cpu_baseline": cpu,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
 
@@ -426,7 +552,10 @@ def main():
         import __graft_entry__
 
         __graft_entry__.build()
-        run_ours(args)
+        if args.op == "copy_blocks":
+            run_copy_blocks(args)
+        else:
+            run_ours(args)
 
 
 if __name__ == "__main__":

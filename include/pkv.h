@@ -74,7 +74,8 @@ typedef enum { PKV_OUT_BF16 = 0, PKV_OUT_FP32 = 1 } pkv_out_dtype;
 /* Device status word bits (pkv_check_device_status). */
 #define PKV_DEVFLAG_BAD_SLOT 0x1u        /* append: slot >= num_blocks * block_size (skipped) */
 #define PKV_DEVFLAG_BAD_CONTEXT_LEN 0x2u /* decode: context length out of range (clamped) */
-#define PKV_DEVFLAG_BAD_BLOCK_ID 0x4u    /* decode: block id outside the pool (read as zeros) */
+#define PKV_DEVFLAG_BAD_BLOCK_ID 0x4u    /* decode: block id outside the pool (read as zeros);
+                                            copy: pair skipped */
 #define PKV_DEVFLAG_WAIT_TIMEOUT 0x8u    /* decode: a pipeline wait hit its iteration limit */
 
 /*
@@ -116,6 +117,22 @@ typedef struct {
 pkv_status pkv_paged_kv_append(const pkv_cache_desc* cache, const void* k, const void* v,
                                const int64_t* slot_mapping, int64_t num_tokens,
                                pkv_stream_t stream);
+
+/*
+ * Copy whole blocks of the pool (copy-on-write; section 4, "Copy-on-Write": sequences that
+ * share a block through reference counts get their own copy before one of them writes into
+ * it, the original staying untouched).
+ *   block_pairs: [num_pairs][2] int64 device array of (src, dst) physical block ids.  For
+ *   each pair, block dst of k_cache and of v_cache becomes a bit copy of block src (all
+ *   block_size slots, every kv head).  src == dst is a no-op.  A pair with an id outside
+ *   [0, num_blocks) is skipped and sets PKV_DEVFLAG_BAD_BLOCK_ID.  If a dst is also a src,
+ *   or two pairs share a dst, the result for those blocks is unspecified.
+ *   num_pairs == 0 is a no-op returning PKV_OK.  The pool description is validated as for
+ *   the append (PKV_ERR_INVALID_ARG before any launch); block_pairs must be 8-byte aligned.
+ *   Asynchronous on stream, like every call here.
+ */
+pkv_status pkv_copy_blocks(const pkv_cache_desc* cache, const int64_t* block_pairs,
+                           int64_t num_pairs, pkv_stream_t stream);
 
 /*
  * Bytes of device workspace that pkv_paged_decode_attention needs for these sizes on the

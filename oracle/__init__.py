@@ -61,6 +61,8 @@ def _L() -> ctypes.CDLL:
         lib.orc_decode_pairs.restype = i32
         lib.orc_decode_pairs.argtypes = [P, P, P, i32, P, i32, i32, i32, i32, P, i32, P, dbl, P, i64,
                                          P, i32]
+        lib.orc_copy_blocks.restype = i32
+        lib.orc_copy_blocks.argtypes = [P, P, i64, i64, P, i64]
         lib.orc_kv_bytes_per_token.restype = i64
         lib.orc_kv_bytes_per_token.argtypes = [i64, i64, i64, i64]
         _lib = lib
@@ -116,6 +118,15 @@ def append(k_cache: np.ndarray, v_cache: np.ndarray, k: np.ndarray, v: np.ndarra
         assert k_cache.dtype == np.uint8 and v_cache.dtype == np.uint8 and sc is not None
     return _L().orc_append(_ptr(k_cache), _ptr(v_cache), nb, bs, hkv, d, kv_dtype, _ptr(k), _ptr(v),
                            _ptr(sm), sm.shape[0], None if sc is None else _ptr(sc))
+
+
+def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs: np.ndarray) -> int:
+    """In-place block copy (copy-on-write) for rows (src, dst) of pairs [n, 2] int64."""
+    assert k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype
+    nb = k_cache.shape[0]
+    block_bytes = k_cache[0].nbytes
+    pr = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    return _L().orc_copy_blocks(_ptr(k_cache), _ptr(v_cache), nb, block_bytes, _ptr(pr), pr.shape[0])
 
 
 def gather(pool: np.ndarray, kv_dtype: int, block_table_row: np.ndarray, length: int, h: int,

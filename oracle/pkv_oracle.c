@@ -149,6 +149,28 @@ int orc_append(void* k_cache, void* v_cache, int64_t num_blocks, int block_size,
   return rc;
 }
 
+/* ---------------------------------------------------------------- copy-on-write */
+
+/* Block copy for copy-on-write ([P1] S4 "Copy-on-Write для parallel sampling": a block
+ * shared by several sequences is copied before one of them writes into it; the original
+ * stays untouched).  For each pair (src, dst): block dst of both pools becomes a byte copy of
+ * block src.  Pairs naming a block outside the pool are skipped; returns -1 if any was. */
+int orc_copy_blocks(void* k_cache, void* v_cache, int64_t num_blocks, int64_t block_bytes,
+                    const int64_t* pairs, int64_t num_pairs) {
+  int rc = 0;
+  for (int64_t p = 0; p < num_pairs; ++p) {
+    int64_t src = pairs[2 * p], dst = pairs[2 * p + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      rc = -1;
+      continue;
+    }
+    if (src == dst) continue;
+    memcpy((char*)k_cache + dst * block_bytes, (const char*)k_cache + src * block_bytes, (size_t)block_bytes);
+    memcpy((char*)v_cache + dst * block_bytes, (const char*)v_cache + src * block_bytes, (size_t)block_bytes);
+  }
+  return rc;
+}
+
 /* ---------------------------------------------------------------- gather */
 
 /* Contiguous fp64 copy of tokens 0..len-1 of one kv head h of one sequence:

@@ -44,6 +44,7 @@ EXPORTED_SYMBOLS = (
     "pkv_paged_kv_append", "pkv_decode_workspace_size", "pkv_decode_workspace_tickets_bytes",
     "pkv_decode_partition_tokens", "pkv_paged_decode_attention", "pkv_check_device_status",
     "pkv_status_string", "pkv_last_error", "pkv_version", "pkv_paged_decode_attention_noalloc",
+    "pkv_copy_blocks",
 )
 
 
@@ -78,6 +79,8 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_decode_attention_noalloc.restype = ctypes.c_int
     lib.pkv_paged_decode_attention_noalloc.argtypes = [ctypes.POINTER(CacheDesc), P, P, i32, P, i32, i32, i32,
                                                        ctypes.c_float, P, ctypes.c_int, P]
+    lib.pkv_copy_blocks.restype = ctypes.c_int
+    lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(CacheDesc), P, i64, P]
     lib.pkv_check_device_status.restype = ctypes.c_int
     lib.pkv_check_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -145,6 +148,18 @@ def paged_kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor
         raise ValueError("k, v must be [num_tokens, num_kv_heads, head_dim]")
     _check(lib.pkv_paged_kv_append(ctypes.byref(desc), k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
                                    _stream(stream)))
+
+
+def copy_blocks(block_pairs: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                scales: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy-on-write: for each row (src, dst) of block_pairs ([n, 2] int64), make block dst
+    of both pools a copy of block src."""
+    desc = _cache_desc(k_cache, v_cache, None, scales)
+    if block_pairs.dtype != torch.int64 or block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise ValueError("block_pairs must be an int64 tensor [n, 2]")
+    if not block_pairs.is_contiguous():
+        raise ValueError("block_pairs must be contiguous")
+    _check(lib.pkv_copy_blocks(ctypes.byref(desc), block_pairs.data_ptr(), block_pairs.shape[0], _stream(stream)))
 
 
 _workspaces: Dict[Tuple[int, int], torch.Tensor] = {}

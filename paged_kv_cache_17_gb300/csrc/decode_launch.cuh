@@ -73,6 +73,11 @@ PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, false)
 PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, true)
 PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, true)
 
+// copy-on-write block copy (copy_blocks.cu)
+cudaError_t launch_copy_blocks(const int64_t* pairs, int64_t num_pairs, int64_t block_bytes, void* k_cache,
+                               void* v_cache, int64_t num_blocks, uint32_t* status, int sm_count,
+                               cudaStream_t stream);
+
 // append (append.cu)
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
                           int hkv, int d, bool fp8, void* k_cache, void* v_cache, int64_t pool_slots,

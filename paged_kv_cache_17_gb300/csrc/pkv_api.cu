@@ -261,6 +261,26 @@ pkv_status pkv_paged_kv_append(const pkv_cache_desc* cache, const void* k, const
   return PKV_OK;
 }
 
+pkv_status pkv_copy_blocks(const pkv_cache_desc* cache, const int64_t* block_pairs, int64_t num_pairs,
+                           pkv_stream_t stream) {
+  t_last_error.clear();
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (num_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "num_pairs must be >= 0");
+  if (num_pairs == 0) return PKV_OK;
+  if (!block_pairs) return fail(PKV_ERR_INVALID_ARG, "block_pairs must be non-NULL");
+  if (!aligned(block_pairs, 8)) return fail(PKV_ERR_INVALID_ARG, "block_pairs must be 8-byte aligned");
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  const int64_t block_bytes = static_cast<int64_t>(cache->block_size) * cache->num_kv_heads * cache->head_dim *
+                              (cache->kv_dtype == PKV_KV_FP8_E4M3 ? 1 : 2);
+  cudaError_t e = pkv::launch_copy_blocks(block_pairs, num_pairs, block_bytes, cache->k_cache, cache->v_cache,
+                                          cache->num_blocks, dev->status, dev->sm_count,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy-blocks launch");
+  return PKV_OK;
+}
+
 int32_t pkv_decode_partition_tokens(int32_t batch, int32_t num_kv_heads, int32_t max_context_len) {
   t_last_error.clear();
   if (batch <= 0 || num_kv_heads <= 0 || max_context_len < 0) {

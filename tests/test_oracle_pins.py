@@ -387,3 +387,29 @@ def test_workload_byte_accounting_uses_the_formula():
                          ("fp8_fork", 2048)):
         c = W.get(name)
         assert oracle.kv_bytes_per_token(1, c.hkv, c.d, c.elem_bytes) == expect
+
+
+# ----------------------------------------------------------------- copy-on-write
+
+def test_copy_blocks_invariants():
+    """A copied block equals its source bit for bit, the source and every other block stay
+    untouched (the pages' copy-on-write: the original remains as it was)."""
+    nb = 10
+    k = rng.integers(0, 2**16, size=(nb, 16, 2, 8), dtype=np.uint16)
+    v = rng.integers(0, 2**16, size=(nb, 16, 2, 8), dtype=np.uint16)
+    k0, v0 = k.copy(), v.copy()
+    pairs = np.array([[1, 7], [4, 4], [2, 9]], dtype=np.int64)
+    assert oracle.copy_blocks(k, v, pairs) == 0
+    for src, dst in ((1, 7), (2, 9)):
+        assert np.array_equal(k[dst], k0[src]) and np.array_equal(v[dst], v0[src])
+    untouched = [i for i in range(nb) if i not in (7, 9)]
+    assert np.array_equal(k[untouched], k0[untouched]) and np.array_equal(v[untouched], v0[untouched])
+    # out-of-range pairs are skipped and reported
+    assert oracle.copy_blocks(k, v, np.array([[0, nb], [-1, 3]], dtype=np.int64)) == -1
+    assert np.array_equal(k[[0, 3]], k0[[0, 3]])
+    # e4m3 pools copy the same way
+    k8 = rng.integers(0, 256, size=(4, 16, 2, 8), dtype=np.uint8)
+    v8 = k8.copy()
+    ref = k8[3].copy()
+    assert oracle.copy_blocks(k8, v8, np.array([[3, 0]], dtype=np.int64)) == 0
+    assert np.array_equal(k8[0], ref)

@@ -138,3 +138,33 @@ def test_unique_bytes_count_shared_blocks_once():
     tails = sum(n - 2048 for n in w.context_lens.tolist())
     assert w.unique_kv_bytes() == (2048 + tails) * per_tok
     assert w.logical_kv_bytes() == w.total_tokens() * per_tok
+
+
+def test_fork_and_copy_on_write_accounting():
+    pool = W.BlockPool(20, generator=torch.Generator().manual_seed(2))
+    a = W.allocate_private(pool, 37)  # 3 blocks, the last holds 5 tokens
+    b = W.fork(pool, a)
+    assert b.blocks == a.blocks and all(pool.ref_cnt[x] == 2 for x in a.blocks)
+    assert pool.num_free == 17
+    # b writes into its shared tail block: it gets a fresh copy, a keeps the original
+    pair = W.copy_on_write(pool, b, 2)
+    assert pair is not None and pair[0] == a.blocks[2] and pair[1] == b.blocks[2] != a.blocks[2]
+    assert pool.ref_cnt[a.blocks[2]] == 1 and pool.ref_cnt[b.blocks[2]] == 1
+    assert pool.num_free == 16
+    # now a's tail is private: no copy
+    assert W.copy_on_write(pool, a, 2) is None
+    # full shared blocks keep being shared
+    assert pool.ref_cnt[a.blocks[0]] == 2
+
+
+def test_contiguous_layout_keeps_lengths_and_orders_ids():
+    s = W.make_workload("llama3_8b")
+    c = W.make_workload("llama3_8b", layout="contiguous")
+    assert torch.equal(s.context_lens, c.context_lens) and s.num_blocks == c.num_blocks
+    nxt = 0
+    for seq in c.seqs:  # sequence after sequence, each one's blocks side by side
+        assert seq.blocks == list(range(nxt, nxt + len(seq.blocks)))
+        nxt += len(seq.blocks)
+    assert s.unique_kv_bytes() == c.unique_kv_bytes()
+    with pytest.raises(ValueError):
+        W.make_workload("tiny", layout="strided")

@@ -119,6 +119,24 @@ def allocate_with_prefix(pool: BlockPool, prefix_blocks: Sequence[int], length: 
     return Sequence_(length, pool.share(prefix_blocks) + pool.allocate(own))
 
 
+def fork(pool: BlockPool, seq: Sequence_) -> Sequence_:
+    """A new sequence sharing every block of seq (parallel sampling / beam search: the
+    pages' copy-on-write paragraph), including a partially filled tail block."""
+    return Sequence_(seq.length, pool.share(seq.blocks))
+
+
+def copy_on_write(pool: BlockPool, seq: Sequence_, logical_block: int):
+    """Before seq writes into its logical block j: if that physical block is shared, give
+    seq a fresh block and return (src, dst) for the device copy; else return None."""
+    blk = seq.blocks[logical_block]
+    if pool.ref_cnt.get(blk, 0) <= 1:
+        return None
+    new = pool.allocate(1)[0]
+    pool.release([blk])
+    seq.blocks[logical_block] = new
+    return blk, new
+
+
 def sampling_token_counts(prompt_tokens: int, generated_tokens: int, samples: int) -> tuple[int, int]:
     """Cached tokens for `samples` parallel samples of one prompt: without sharing
     (every sample keeps its own copy of the prompt) and with the prompt shared."""

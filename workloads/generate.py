@@ -132,7 +132,8 @@ def _lengths(cfg: Config, g: torch.Generator) -> List[int]:
     return [cfg.prefix_len + t for t in draws]  # prefix / fork: shared part + private tail
 
 
-def _build_sequences(cfg: Config, lens: List[int], g: torch.Generator) -> tuple[BlockPool, List[Sequence_]]:
+def _build_sequences(cfg: Config, lens: List[int], g: torch.Generator,
+                     contiguous: bool = False) -> tuple[BlockPool, List[Sequence_]]:
     bs = BLOCK_SIZE
     if cfg.kind in ("prefix", "fork"):
         assert cfg.prefix_len % bs == 0, "only full blocks are shared"
@@ -143,7 +144,9 @@ def _build_sequences(cfg: Config, lens: List[int], g: torch.Generator) -> tuple[
         used = sum(blocks_for_tokens(n, bs) for n in lens)
     nb = cfg.pool_blocks if cfg.pool_blocks is not None else int(math.ceil(used * (1.0 + cfg.spare_frac)))
     assert nb >= used
-    pool = BlockPool(nb, bs, generator=g)
+    # shuffled: ids come from a seeded permutation, so consecutive logical blocks land
+    # anywhere; contiguous: ids in order, each sequence's blocks side by side in the pool
+    pool = BlockPool(nb, bs, generator=None if contiguous else g)
     seqs: List[Sequence_] = []
     if cfg.kind in ("explicit", "uniform"):
         seqs = [allocate_private(pool, n) for n in lens]
@@ -162,8 +165,12 @@ def _build_sequences(cfg: Config, lens: List[int], g: torch.Generator) -> tuple[
 
 
 def make_workload(cfg_or_name, seed: Optional[int] = None, lens: Optional[List[int]] = None,
-                  threads: int = 8) -> Workload:
-    """Build one seeded workload.  `lens` overrides the drawn lengths (same structure)."""
+                  threads: int = 8, layout: str = "shuffled") -> Workload:
+    """Build one seeded workload.  `lens` overrides the drawn lengths (same structure).
+    layout "contiguous" hands out block ids in order instead of shuffled (the same lengths
+    and sharing; the pool values then sit at other physical ids)."""
+    if layout not in ("shuffled", "contiguous"):
+        raise ValueError(f"layout must be 'shuffled' or 'contiguous', not {layout!r}")
     cfg = cfg_or_name if isinstance(cfg_or_name, Config) else get(cfg_or_name)
     seed = cfg.seed if seed is None else seed
     g = torch.Generator().manual_seed(seed)
@@ -171,7 +178,7 @@ def make_workload(cfg_or_name, seed: Optional[int] = None, lens: Optional[List[i
     if lens is not None:
         assert len(lens) == len(drawn)
         drawn = list(lens)
-    pool, seqs = _build_sequences(cfg, drawn, g)
+    pool, seqs = _build_sequences(cfg, drawn, g, contiguous=(layout == "contiguous"))
     nb = pool.num_blocks
     B = len(seqs)
     M = max(len(s.blocks) for s in seqs)
