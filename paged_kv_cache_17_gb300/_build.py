@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libpkv.so")
-SOURCES = ["pkv_api.cu", "append.cu", "decode_bf16.cu", "decode_e4m3.cu", "pkv_noalloc.cu", "copy_blocks.cu"]
+SOURCES = ["pkv_api.cu", "append.cu", "decode_bf16.cu", "decode_e4m3.cu", "pkv_noalloc.cu", "copy_blocks.cu",
+           "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -36,7 +37,9 @@ def _stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "pkv.h"), __file__]
+    inc = os.path.join(ROOT, "include")
+    deps = ([os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(inc, f) for f in os.listdir(inc)]
+            + [__file__])
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
@@ -50,7 +53,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     cc = nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *_flags(extra_flags), "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -19,19 +19,24 @@ def pkv():
     return m
 
 
-def header_functions():
-    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+def header_functions(name):
+    text = open(os.path.join(ROOT, "include", name)).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_symbols_are_exported(pkv):
-    names = header_functions()
-    assert len(names) >= 9
+    from paged_kv_cache_17_gb300 import block_manager
+
+    headers = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    assert headers == ["pkv.h", "pkv_block_manager.h"]
     lib = ctypes.CDLL(pkv.LIB_PATH)
-    for n in names:
-        assert hasattr(lib, n), f"{n} declared in include/pkv.h but not exported"
-    assert set(names) == set(pkv.EXPORTED_SYMBOLS)
+    for h, bound in (("pkv.h", pkv.EXPORTED_SYMBOLS), ("pkv_block_manager.h", block_manager.EXPORTED_SYMBOLS)):
+        names = header_functions(h)
+        assert len(names) >= 9
+        for n in names:
+            assert hasattr(lib, n), f"{n} declared in include/{h} but not exported"
+        assert set(names) == set(bound)
 
 
 def test_version_and_status_strings(pkv):
