@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--layout", default="shuffled", choices=["shuffled", "contiguous"],
                     help="physical block order of the pool (contiguous = each sequence's blocks in order)")
     ap.add_argument("--copy-pairs", type=int, default=4096, help="(src, dst) pairs per copy_blocks launch")
+    ap.add_argument("--cascade", action="store_true",
+                    help="decode through the cascade call: shared prefixes once for all their members "
+                         "(tensor cores), each sequence's own blocks by the decode kernel")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -249,16 +252,35 @@ def run_ours(args):
          dict(q=w.q, k_cache=w.k_cache, v_cache=w.v_cache, k_new=w.k_new, v_new=w.v_new, slots=w.slot_mapping,
               tables=w.block_tables, lens=w.context_lens, scales=w.scales).items()}
     out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=dev)
-    need = pkv.workspace_size(B, hq, hkv, d, max_len)
+    cas = w.cascade() if args.cascade else None
+    if cas is not None:
+        ct = {k: getattr(cas, k).to(dev) for k in ("prefix_tables", "prefix_lens", "member_indptr", "member_seqs",
+                                                    "seq_prefix", "block_tables", "context_lens")}
+        suffix_max = max(16, int(cas.context_lens.max()))
+        need = pkv.cascade_workspace_size(B, hq, hkv, d, suffix_max, cas.prefix_tables.shape[0], cas.max_members,
+                                          cas.max_prefix_len)
+    else:
+        need = pkv.workspace_size(B, hq, hkv, d, max_len)
     wsbuf = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    def decode(q, tables, lens, ctabs=None):
+        if cas is None:
+            pkv.paged_decode_attention(q, t["k_cache"], t["v_cache"], tables, lens, cfg.softmax_scale, out,
+                                       scales=t["scales"], max_context_len=max_len, workspace=wsbuf)
+        else:
+            c2 = ctabs or ct
+            pkv.cascade_decode_attention(q, t["k_cache"], t["v_cache"], c2["prefix_tables"], c2["prefix_lens"],
+                                         c2["member_indptr"], c2["member_seqs"], c2["seq_prefix"], c2["block_tables"],
+                                         c2["context_lens"], cfg.softmax_scale, out, max_members=cas.max_members,
+                                         max_prefix_len=cas.max_prefix_len, max_context_len=suffix_max,
+                                         scales=t["scales"], workspace=wsbuf)
+
     def step():
         pkv.paged_kv_append(t["k_new"], t["v_new"], t["slots"], t["k_cache"], t["v_cache"], scales=t["scales"])
         mid.record(stream)
-        pkv.paged_decode_attention(t["q"], t["k_cache"], t["v_cache"], t["tables"], t["lens"], cfg.softmax_scale,
-                                   out, scales=t["scales"], max_context_len=max_len, workspace=wsbuf)
+        decode(t["q"], t["tables"], t["lens"])
 
     mid = torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
@@ -320,8 +342,11 @@ def run_ours(args):
     # ---- end to end through the public API with host buffers (pinned), H2D + D2H timed
     e2e = None
     if not args.no_e2e:
-        host = {k: v.pin_memory() for k, v in dict(q=w.q, k_new=w.k_new, v_new=w.v_new, slots=w.slot_mapping,
-                                                     tables=w.block_tables, lens=w.context_lens).items()}
+        inputs = dict(q=w.q, k_new=w.k_new, v_new=w.v_new, slots=w.slot_mapping, tables=w.block_tables,
+                      lens=w.context_lens)
+        if cas is not None:
+            inputs.update({"c_" + k: getattr(cas, k) for k in ct})
+        host = {k: v.pin_memory() for k, v in inputs.items()}
         h_out = torch.empty((B, hq, d), dtype=torch.bfloat16).pin_memory()
         dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
         h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -332,9 +357,8 @@ def run_ours(args):
                 dev_in[k].copy_(v, non_blocking=True)
             pkv.paged_kv_append(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], t["k_cache"], t["v_cache"],
                                 scales=t["scales"])
-            pkv.paged_decode_attention(dev_in["q"], t["k_cache"], t["v_cache"], dev_in["tables"], dev_in["lens"],
-                                       cfg.softmax_scale, out, scales=t["scales"], max_context_len=max_len,
-                                       workspace=wsbuf)
+            ctabs = {k[2:]: v for k, v in dev_in.items() if k.startswith("c_")} if cas is not None else None
+            decode(dev_in["q"], dev_in["tables"], dev_in["lens"], ctabs)
             h_out.copy_(out, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -377,19 +401,20 @@ def run_ours(args):
                    "batch": B, "num_q_heads": hq, "num_kv_heads": hkv, "head_dim": d, "kv_dtype": cfg.kv_dtype,
                    "max_context_len": max_len, "total_context_tokens": w.total_tokens(),
                    "partition_tokens": pkv.partition_tokens(B, hkv, max_len),
-                   "layout": args.layout,
+                   "layout": args.layout, "decode_call": "cascade" if cas is not None else "paged",
                    "l2": "flushed between timed steps (256 MiB write, untimed)", "parallelism": f"replicas x{ws}"},
         "us_per_step": round(ms_per_step * 1e3, 2),
         "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
         "bytes_per_step": nb,
         "decode_us": round(dec_avg_ms * 1e3, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": ncu_traffic(cfg.name),
-                     "kernel": "paged_decode_kernel", "peak_source": f"{peak_src} hbm_gbs (copy)",
+                     "frac": round(achieved / peak, 4), "traffic": None if cas is not None else ncu_traffic(cfg.name),
+                     "kernel": "cascade_prefix_kernel + paged_decode_kernel" if cas is not None else "paged_decode_kernel",
+                     "peak_source": f"{peak_src} hbm_gbs (copy)",
                      "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if cas is not None and cas.prefix_tables.shape[0] > 0 else 2) * args.steps,
         "clocks": clocks,
         "wall_s": round(wall, 3),
     }

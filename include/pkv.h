@@ -210,6 +210,57 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const
                                               pkv_out_dtype out_dtype, pkv_stream_t stream);
 
 /*
+ * Two-level (cascade) decode attention for sequences that share a prompt prefix.
+ * (section 7, "Тот самый Cache Read": requests with the same prompt read the same cached
+ * prefix blocks; section 3: attention over a split of the keys into parts is recovered
+ * exactly from each part's running max, running sum and unnormalised output.)
+ * The result for every (b, hq) is the decode attention of q[b][hq] over the concatenation
+ * (prefix blocks of sequence b, if any) then (the blocks of block_tables row b), exactly
+ * as pkv_paged_decode_attention over that concatenated table computes it, up to fp32
+ * rounding.  The prefix part is computed once per prefix for all its member sequences,
+ * as a dense [members x G rows] x [prefix keys] contraction on the tensor cores
+ * (mma.sync, bf16 in, fp32 accumulate); the sequences' own blocks go through the decode
+ * kernel, which merges the prefix results with log-sum-exp weights.
+ *   prefixes: see pkv_prefix_desc; may describe zero prefixes (then this is a plain decode).
+ *   block_tables / context_lens: each sequence's blocks AFTER its prefix and their token
+ *     count (its full table and length when it has no prefix); 0 is allowed when the
+ *     prefix is the whole context.
+ *   Other arguments as for pkv_paged_decode_attention; workspace of at least
+ *   pkv_cascade_workspace_size(...) bytes (never 0 when prefixes exist), same zero-ticket
+ *   contract.  E4M3 pools: the prefix pass expands the codes exactly to fp16 and multiplies
+ *   in fp16 (q rounded to fp16, exact for |q| in 2^-14 .. 65504).  Both pools round the
+ *   prefix softmax weights to the MMA's 16-bit type before the P V product.
+ */
+typedef struct {
+  const int32_t* prefix_tables;  /* [num_prefixes][max_prefix_blocks] physical block ids */
+  int32_t max_prefix_blocks;
+  const int32_t* prefix_lens;    /* [num_prefixes] tokens, each a multiple of 16 (whole
+                                    blocks are shared) and <= max_prefix_len */
+  int32_t num_prefixes;
+  const int32_t* member_indptr;  /* [num_prefixes + 1]: the members of prefix p are */
+  const int32_t* member_seqs;    /* member_seqs[member_indptr[p] .. member_indptr[p+1]) */
+  int32_t max_members;           /* upper bound on the members of one prefix */
+  int32_t max_prefix_len;        /* upper bound on prefix_lens (tokens) */
+  const int32_t* seq_prefix;     /* [batch]: p for a member of prefix p, else -1; every
+                                    sequence belongs to at most one prefix and must appear
+                                    in that prefix's member list */
+} pkv_prefix_desc;
+
+size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t max_context_len,
+                                  int32_t num_prefixes, int32_t max_members,
+                                  int32_t max_prefix_len);
+
+pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void* q,
+                                        const pkv_prefix_desc* prefixes,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t batch,
+                                        int32_t num_q_heads, int32_t max_context_len,
+                                        float softmax_scale, void* out, pkv_out_dtype out_dtype,
+                                        void* workspace, size_t workspace_bytes,
+                                        pkv_stream_t stream);
+
+/*
  * Read and clear the device status word of the current device after the work queued on
  * `stream` so far has finished (this call synchronises `stream`).  *flags receives the
  * PKV_DEVFLAG_* bits (may be NULL).  Returns PKV_ERR_DEVICE_CHECK if any bit was set,

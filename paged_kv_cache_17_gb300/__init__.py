@@ -44,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "pkv_paged_kv_append", "pkv_decode_workspace_size", "pkv_decode_workspace_tickets_bytes",
     "pkv_decode_partition_tokens", "pkv_paged_decode_attention", "pkv_check_device_status",
     "pkv_status_string", "pkv_last_error", "pkv_version", "pkv_paged_decode_attention_noalloc",
-    "pkv_copy_blocks",
+    "pkv_copy_blocks", "pkv_cascade_workspace_size", "pkv_cascade_decode_attention",
 )
 
 
@@ -58,6 +58,14 @@ class CacheDesc(ctypes.Structure):
     _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
                 ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int), ("scales", ctypes.c_void_p)]
+
+
+class PrefixDesc(ctypes.Structure):
+    _fields_ = [("prefix_tables", ctypes.c_void_p), ("max_prefix_blocks", ctypes.c_int32),
+                ("prefix_lens", ctypes.c_void_p), ("num_prefixes", ctypes.c_int32),
+                ("member_indptr", ctypes.c_void_p), ("member_seqs", ctypes.c_void_p),
+                ("max_members", ctypes.c_int32), ("max_prefix_len", ctypes.c_int32),
+                ("seq_prefix", ctypes.c_void_p)]
 
 
 def _load() -> ctypes.CDLL:
@@ -79,6 +87,11 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_decode_attention_noalloc.restype = ctypes.c_int
     lib.pkv_paged_decode_attention_noalloc.argtypes = [ctypes.POINTER(CacheDesc), P, P, i32, P, i32, i32, i32,
                                                        ctypes.c_float, P, ctypes.c_int, P]
+    lib.pkv_cascade_workspace_size.restype = sz
+    lib.pkv_cascade_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32]
+    lib.pkv_cascade_decode_attention.restype = ctypes.c_int
+    lib.pkv_cascade_decode_attention.argtypes = [ctypes.POINTER(CacheDesc), P, ctypes.POINTER(PrefixDesc), P, i32, P,
+                                                 i32, i32, i32, ctypes.c_float, P, ctypes.c_int, P, sz, P]
     lib.pkv_copy_blocks.restype = ctypes.c_int
     lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(CacheDesc), P, i64, P]
     lib.pkv_check_device_status.restype = ctypes.c_int
@@ -226,6 +239,67 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     _check(lib.pkv_paged_decode_attention(ctypes.byref(desc), q.data_ptr(), block_tables.data_ptr(), max_blocks,
                                           context_lens.data_ptr(), B, hq, max_context_len, float(softmax_scale),
                                           out.data_ptr(), out_code, ws_ptr, ws_bytes, sh))
+    return out
+
+
+def cascade_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_context_len: int,
+                           num_prefixes: int, max_members: int, max_prefix_len: int) -> int:
+    return int(lib.pkv_cascade_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_context_len,
+                                              num_prefixes, max_members, max_prefix_len))
+
+
+def cascade_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             prefix_tables: torch.Tensor, prefix_lens: torch.Tensor, member_indptr: torch.Tensor,
+                             member_seqs: torch.Tensor, seq_prefix: torch.Tensor, block_tables: torch.Tensor,
+                             context_lens: torch.Tensor, softmax_scale: float, out: Optional[torch.Tensor] = None, *,
+                             max_members: int, max_prefix_len: Optional[int] = None,
+                             max_context_len: Optional[int] = None, scales: Optional[torch.Tensor] = None,
+                             workspace: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Decode attention where sequences share prefixes: prefix p ([num_prefixes] rows of
+    prefix_tables, prefix_lens[p] tokens) is attended once for all its members
+    member_seqs[member_indptr[p]:member_indptr[p+1]]; block_tables / context_lens hold each
+    sequence's blocks after its prefix (seq_prefix[b] = p, or -1 without a prefix)."""
+    desc = _cache_desc(k_cache, v_cache, None, scales)
+    if q.dtype != torch.bfloat16 or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be a contiguous bfloat16 tensor [B, Hq, D]")
+    B, hq, d = q.shape
+    for name, t in (("prefix_tables", prefix_tables), ("prefix_lens", prefix_lens), ("member_indptr", member_indptr),
+                    ("member_seqs", member_seqs), ("seq_prefix", seq_prefix), ("block_tables", block_tables),
+                    ("context_lens", context_lens)):
+        if t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous int32 tensor")
+    if prefix_tables.dim() != 2 or prefix_lens.shape != (prefix_tables.shape[0],):
+        raise ValueError("prefix_tables must be [P, max_prefix_blocks] and prefix_lens [P]")
+    P = prefix_tables.shape[0]
+    if member_indptr.shape != (P + 1,) or seq_prefix.shape != (B,):
+        raise ValueError("member_indptr must be [P + 1] and seq_prefix [B]")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, max_blocks] and context_lens [B]")
+    if max_prefix_len is None:
+        max_prefix_len = prefix_tables.shape[1] * 16
+    if max_context_len is None:
+        max_context_len = block_tables.shape[1] * 16
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=q.device)
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (B, hq, d) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B, Hq, D] bfloat16 or float32 tensor")
+    px = PrefixDesc(prefix_tables.data_ptr(), prefix_tables.shape[1], prefix_lens.data_ptr(), P,
+                    member_indptr.data_ptr(), member_seqs.data_ptr() if member_seqs.numel() else None,
+                    max_members, max_prefix_len, seq_prefix.data_ptr())
+    sh = _stream(stream)
+    need = cascade_workspace_size(B, hq, desc.num_kv_heads, d, max_context_len, P, max_members, max_prefix_len)
+    if need == 0 and lib.pkv_last_error():
+        raise PkvError(PKV_ERR_INVALID_ARG, lib.pkv_last_error().decode())
+    ws_ptr, ws_bytes = None, 0
+    if need > 0:
+        ws = workspace if workspace is not None else _workspace(q.device, sh, need)
+        ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    _check(lib.pkv_cascade_decode_attention(ctypes.byref(desc), q.data_ptr(), ctypes.byref(px),
+                                            block_tables.data_ptr(), block_tables.shape[1], context_lens.data_ptr(),
+                                            B, hq, max_context_len, float(softmax_scale), out.data_ptr(),
+                                            OUT_FP32 if out.dtype == torch.float32 else OUT_BF16, ws_ptr, ws_bytes,
+                                            sh))
     return out
 
 

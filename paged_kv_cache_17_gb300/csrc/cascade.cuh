@@ -1,0 +1,47 @@
+// cascade.cuh -- parameters and launch of the shared-prefix pass of cascade decode.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace pkv {
+
+struct PrefixParams {
+  const uint16_t* q;             // [B][Hq][D] bf16
+  const int32_t* prefix_tables;  // [P][max_prefix_blocks]
+  const int32_t* prefix_lens;    // [P], tokens, multiples of 16
+  const int32_t* indptr;         // [P + 1]: members of prefix p are seqs[indptr[p] .. indptr[p+1])
+  const int32_t* seqs;           // member sequence ids
+  float* part_ml;                // records [B][Hkv][rec_slots][G][2]
+  float* part_acc;               // records [B][Hkv][rec_slots][G][D]
+  uint32_t* status;
+  int max_prefix_blocks;
+  int max_members;  // grid coverage: members per prefix
+  int batch;
+  int hq;
+  int hkv;
+  int group;        // G = Hq / Hkv
+  int num_blocks;   // pool size in blocks
+  int split_blocks; // prefix blocks per split (a multiple of 4)
+  int pre_slots;    // splits per prefix = prefix records per (sequence, kv head)
+  int rec_slots;    // records per (sequence, kv head): pre_slots + decode partitions
+  float score_scale;  // softmax_scale * log2(e)
+  const float* scales;  // [2][Hkv] (E4M3 pools) or nullptr
+};
+
+// bf16 pools take the 128-byte-swizzled 64-column tensor maps, E4M3 pools the plain ones
+template <int D, bool FP8>
+cudaError_t launch_cascade_prefix(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p, dim3 grid,
+                                  cudaStream_t stream, int device);
+#define PKV_DECLARE_PREFIX(D, FP8)                                                                              \
+  extern template cudaError_t launch_cascade_prefix<D, FP8>(const CUtensorMap&, const CUtensorMap&,            \
+                                                            const PrefixParams&, dim3, cudaStream_t, int);
+PKV_DECLARE_PREFIX(64, false)
+PKV_DECLARE_PREFIX(128, false)
+PKV_DECLARE_PREFIX(64, true)
+PKV_DECLARE_PREFIX(128, true)
+#undef PKV_DECLARE_PREFIX
+
+}  // namespace pkv

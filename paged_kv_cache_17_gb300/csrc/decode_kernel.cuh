@@ -44,8 +44,9 @@ struct DecodeParams {
   const float* scales;          // [2][Hkv] (E4M3) or nullptr
   void* out;                    // [B][Hq][D] bf16 or fp32
   int32_t* tickets;             // [B][Hkv]        (multi-partition only)
-  float* part_ml;               // [B][Hkv][S][G][2]
-  float* part_acc;              // [B][Hkv][S][G][D]
+  float* part_ml;               // [B][Hkv][rec_slots][G][2]
+  float* part_acc;              // [B][Hkv][rec_slots][G][D]
+  const int32_t* seq_prefix;    // [B]: >= 0 if the sequence has shared-prefix records, or nullptr
   uint32_t* status;
   int max_blocks;
   int hq;
@@ -54,6 +55,8 @@ struct DecodeParams {
   int max_context_len;  // launch bound on context_lens
   int split_blocks;     // blocks per partition
   int max_splits;       // gridDim.z
+  int pre_slots;        // shared-prefix records per (b, h) ahead of the partitions' (0: none)
+  int rec_slots;        // records per (b, h): pre_slots + max_splits
   float score_scale;    // softmax_scale * log2(e)
   int out_fp32;
 };
@@ -248,6 +251,47 @@ __device__ __forceinline__ void consume_block(const uint8_t* kt, const uint8_t* 
   __syncwarp();  // the next block rewrites pbuf
 }
 
+// Final output of (b, h) from its partial records lo .. hi-1 (log2-domain max, sum and
+// unnormalised output per query head), combined in record order with their log-sum-exp
+// weights (deterministic).  All threads of the CTA take part; wts is shared scratch of
+// G * (rec_slots + 1) floats.  A head whose records are all empty gets zeros.
+template <int D, int G, bool FP8>
+__device__ __forceinline__ void merge_records(const DecodeParams& p, int b, int h, int lo, int hi, float* wts,
+                                              int nthreads) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = nthreads >> 5;
+  const size_t rec0 = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots;
+  const int R = p.rec_slots;
+  for (int g = warp; g < G; g += nwarps) {
+    float M = -INFINITY;
+    for (int j = lo + lane; j < hi; j += 32) M = fmaxf(M, __ldcg(&p.part_ml[((rec0 + j) * G + g) * 2]));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, shfl_xor(M, m));
+    for (int j = lo + lane; j < hi; j += 32)
+      wts[g * R + j] = M == -INFINITY ? 0.f : fast_exp2(__ldcg(&p.part_ml[((rec0 + j) * G + g) * 2]) - M);
+    __syncwarp();
+    if (lane == 0) {  // the denominator is summed in record order (deterministic)
+      float den = 0.f;
+      for (int j = lo; j < hi; ++j) den = fmaf(wts[g * R + j], __ldcg(&p.part_ml[((rec0 + j) * G + g) * 2 + 1]), den);
+      wts[G * R + g] = den > 0.f ? 1.0f / den : 0.f;
+    }
+  }
+  __syncthreads();
+  float vfix = 1.0f;  // E4M3 values carry 2^-120; V's scale and that factor go to the output
+  if constexpr (FP8) vfix = p.scales[p.hkv + h];
+  const size_t out_row0 = static_cast<size_t>(b) * p.hq + h * G;
+  for (int e = threadIdx.x; e < G * D; e += nthreads) {
+    const int g = e / D, d = e % D;
+    float num = 0.f;
+    for (int j = lo; j < hi; ++j) num = fmaf(wts[g * R + j], __ldcg(&p.part_acc[((rec0 + j) * G + g) * D + d]), num);
+    float o = num * wts[G * R + g];
+    if constexpr (FP8) o = (o * 1152921504606846976.0f) * (vfix * 1152921504606846976.0f);  // 2^60 * 2^60
+    const size_t oi = (out_row0 + g) * D + d;
+    if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
+    else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+  }
+}
+
 template <int D, int G, bool FP8, int NWC, int STAGES>
 __global__ void __launch_bounds__((NWC + 1) * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -270,7 +314,12 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  pdl_wait();  // no global reads before the preceding kernel (e.g. the append) completed
+  // No global reads before the preceding kernel (e.g. the append) completed.  In a cascade
+  // call the preceding kernel is the prefix pass, which lets this grid start once all its
+  // CTAs are past their own wait (so the append's results are visible); this kernel then
+  // waits for the prefix pass itself only before it reads the prefix records.
+  const bool cascade = p.seq_prefix != nullptr;
+  if (!cascade) pdl_wait();
 
   // ---- sequence length (checked, clamped) and this CTA's share of it
   int len = p.context_lens[b];
@@ -285,12 +334,19 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
   const int hq0 = h * G;
 
-  if (nblk == 0) {  // empty sequence: zero output, written by partition 0
+  // shared-prefix records (written by the prefix pass) come first among this (b, h)'s records
+  const int npre = (p.seq_prefix != nullptr && p.seq_prefix[b] >= 0) ? p.pre_slots : 0;
+  if (nblk == 0) {  // no own blocks: partition 0 writes zeros, or the prefix result alone
     if (s == 0) {
-      for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
-        const size_t o = (static_cast<size_t>(b) * p.hq + hq0) * D + e;
-        if (p.out_fp32) reinterpret_cast<float*>(p.out)[o] = 0.f;
-        else reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
+      if (npre > 0) {
+        pdl_wait();
+        merge_records<D, G, FP8>(p, b, h, 0, npre, reinterpret_cast<float*>(smem), C::kThreads);
+      } else {
+        for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
+          const size_t o = (static_cast<size_t>(b) * p.hq + hq0) * D + e;
+          if (p.out_fp32) reinterpret_cast<float*>(p.out)[o] = 0.f;
+          else reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
+        }
       }
     }
     return;
@@ -447,7 +503,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   const size_t out_row0 = static_cast<size_t>(b) * p.hq + hq0;
   float vfix = 1.0f;  // E4M3 values carry 2^-120; V's scale and that factor go to the output
   if constexpr (FP8) vfix = p.scales[p.hkv + h];
-  const bool single = (nsplit == 1);
+  const bool single = (nsplit == 1 && npre == 0);
+  // one partition and prefix records: merge them right here (no record, no ticket)
+  const bool with_prefix = (nsplit == 1 && npre > 0);
+  if (with_prefix) pdl_wait();
+  const size_t prec0 = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots;
   for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
     const int g = e / D, d = e % D;
     const int ghg = g / GW, gw = g % GW;
@@ -462,14 +522,34 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       num = fmaf(wt, aw[(w * GW + gw) * D + d], num);
       den = fmaf(wt, lw[w * GW + gw], den);
     }
-    if (single) {
+    if (with_prefix) {
+      // combine with the prefix records in record order: theirs, then this partition's
+      float Mt = M;
+      for (int j = 0; j < npre; ++j) Mt = fmaxf(Mt, __ldcg(&p.part_ml[((prec0 + j) * G + g) * 2]));
+      float num2 = 0.f, den2 = 0.f;
+      if (Mt != -INFINITY) {
+        for (int j = 0; j < npre; ++j) {
+          const float wj = fast_exp2(__ldcg(&p.part_ml[((prec0 + j) * G + g) * 2]) - Mt);
+          num2 = fmaf(wj, __ldcg(&p.part_acc[((prec0 + j) * G + g) * D + d]), num2);
+          den2 = fmaf(wj, __ldcg(&p.part_ml[((prec0 + j) * G + g) * 2 + 1]), den2);
+        }
+        const float ws = fast_exp2(M - Mt);
+        num2 = fmaf(ws, num, num2);
+        den2 = fmaf(ws, den, den2);
+      }
+      float o = den2 > 0.f ? num2 / den2 : 0.f;
+      if constexpr (FP8) o = (o * 1152921504606846976.0f) * (vfix * 1152921504606846976.0f);  // 2^60 * 2^60
+      const size_t oi = (out_row0 + g) * D + d;
+      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
+      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+    } else if (single) {
       float o = num / den;
       if constexpr (FP8) o = (o * 1152921504606846976.0f) * (vfix * 1152921504606846976.0f);  // 2^60 * 2^60
       const size_t oi = (out_row0 + g) * D + d;
       if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
       else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
     } else {
-      const size_t rec = (static_cast<size_t>(b) * p.hkv + h) * p.max_splits + s;
+      const size_t rec = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots + p.pre_slots + s;
       p.part_acc[(rec * G + g) * D + d] = num;
       if (d == 0) {
         p.part_ml[(rec * G + g) * 2 + 0] = M;
@@ -477,7 +557,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       }
     }
   }
-  if (single) return;
+  if (single || with_prefix) return;
 
   // ================================================================ cross-partition merge
   __shared__ int s_last;
@@ -490,37 +570,10 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // weights per (g, partition) in the tile area: w[g][s] = 2^(m_s - M_g) / sum_s 2^(m_s - M_g) l_s
-  float* wts = reinterpret_cast<float*>(smem);
-  const size_t rec0 = (static_cast<size_t>(b) * p.hkv + h) * p.max_splits;
-  for (int g = warp; g < G; g += NWC + 1) {
-    float M = -INFINITY;
-    for (int j = lane; j < nsplit; j += 32) M = fmaxf(M, __ldcg(&p.part_ml[((rec0 + j) * G + g) * 2]));
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, shfl_xor(M, m));
-    // the denominator is summed in partition order by lane 0 (deterministic)
-    for (int j = lane; j < nsplit; j += 32)
-      wts[g * p.max_splits + j] = fast_exp2(__ldcg(&p.part_ml[((rec0 + j) * G + g) * 2]) - M);
-    __syncwarp();
-    if (lane == 0) {
-      float den = 0.f;
-      for (int j = 0; j < nsplit; ++j)
-        den = fmaf(wts[g * p.max_splits + j], __ldcg(&p.part_ml[((rec0 + j) * G + g) * 2 + 1]), den);
-      wts[G * p.max_splits + g] = 1.0f / den;
-    }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
-    const int g = e / D, d = e % D;
-    float num = 0.f;
-    for (int j = 0; j < nsplit; ++j)
-      num = fmaf(wts[g * p.max_splits + j], __ldcg(&p.part_acc[((rec0 + j) * G + g) * D + d]), num);
-    float o = num * wts[G * p.max_splits + g];
-    if constexpr (FP8) o = (o * 1152921504606846976.0f) * (vfix * 1152921504606846976.0f);
-    const size_t oi = (out_row0 + g) * D + d;
-    if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
-    else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-  }
+  if (npre > 0) pdl_wait();
+  // this sequence's records: the prefix pass's (if any), then one per partition
+  merge_records<D, G, FP8>(p, b, h, p.pre_slots - npre, p.pre_slots + nsplit, reinterpret_cast<float*>(smem),
+                           C::kThreads);
   if (threadIdx.x == 0) p.tickets[b * p.hkv + h] = 0;  // leave the ticket region zero
 }
 

@@ -13,6 +13,7 @@
 #include <string>
 
 #include "../../include/pkv.h"
+#include "cascade.cuh"
 #include "decode_launch.cuh"
 
 namespace {
@@ -157,21 +158,24 @@ struct WsLayout {
   size_t tickets, ml, acc, total;
 };
 
-WsLayout ws_layout(int batch, int hkv, int g, int d, const Split& sp) {
+// Partial records per (sequence, kv head): pre_slots from a shared-prefix pass, then one per
+// context partition.  A plain decode with one partition needs no workspace.
+WsLayout ws_layout(int batch, int hkv, int g, int d, const Split& sp, int pre_slots) {
   WsLayout w{0, 0, 0, 0};
-  if (sp.max_splits <= 1) return w;
+  if (sp.max_splits <= 1 && pre_slots == 0) return w;
   const size_t units = static_cast<size_t>(batch) * hkv;
+  const size_t slots = static_cast<size_t>(pre_slots) + sp.max_splits;
   w.tickets = static_cast<size_t>(kTickets) * sizeof(int32_t);
-  w.ml = round256(units * sp.max_splits * g * 2 * sizeof(float));
-  w.acc = round256(units * sp.max_splits * g * d * sizeof(float));
+  w.ml = round256(units * slots * g * 2 * sizeof(float));
+  w.acc = round256(units * slots * g * d * sizeof(float));
   w.total = w.tickets + w.ml + w.acc;
   return w;
 }
 
-// Merge weights of one (b, h) use G * max_splits + G floats of the tile area.
-Split fit_split(Split sp, int g, int max_context_len, int tile_area_bytes) {
+// Merge weights of one (b, h) use G * (records + 1) floats of the tile area.
+Split fit_split(Split sp, int g, int max_context_len, int tile_area_bytes, int pre_slots) {
   const int max_nblk = (max_context_len + 15) / 16;
-  while (sp.max_splits > 1 && static_cast<long long>(g) * (sp.max_splits + 1) * 4 > tile_area_bytes) {
+  while (sp.max_splits > 1 && static_cast<long long>(g) * (pre_slots + sp.max_splits + 1) * 4 > tile_area_bytes) {
     sp.split_blocks *= 2;
     if (sp.split_blocks > max_nblk) sp.split_blocks = max_nblk;
     sp.max_splits = (max_nblk + sp.split_blocks - 1) / sp.split_blocks;
@@ -190,6 +194,54 @@ bool encode_kv_map(CUtensorMap* tm, void* base, int64_t num_blocks, int hkv, int
                               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// The same pool view with 64-element (128-byte) boxes of 16 rows, 128-byte swizzled: the
+// tile layout the tensor-core prefix pass reads with ldmatrix (bf16 pools only).
+bool encode_kv_map_sw128(CUtensorMap* tm, void* base, int64_t num_blocks, int hkv, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                              static_cast<cuuint64_t>(num_blocks) * 16};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(hkv) * d * 2};
+  const cuuint32_t box[3] = {64, 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Splits of the prefix pass: each split is a run of whole 64-key stages (a multiple of four
+// blocks), at least two stages long; the count minimises (waves of CTAs, two resident per
+// SM) x (blocks per split + 8), the 8 blocks standing for a CTA's start-up and the merge
+// work every extra record adds; the fewest splits on a tie.
+struct PrefixPlan {
+  int tiles;         // 64-row query tiles per prefix
+  int pre_slots;     // splits per prefix
+  int split_blocks;  // prefix blocks per split
+};
+
+PrefixPlan plan_prefix(int num_prefixes, int max_members, int max_prefix_len, int g, int hkv, int sm_count) {
+  PrefixPlan pp{0, 0, 0};
+  const int pblocks = (max_prefix_len + 15) / 16;
+  if (num_prefixes <= 0 || max_members <= 0 || pblocks <= 0) return pp;
+  pp.tiles = static_cast<int>((static_cast<long long>(max_members) * g + 63) / 64);
+  const long long per_split = static_cast<long long>(pp.tiles) * hkv * num_prefixes;
+  const long long slots = 2LL * sm_count;
+  const int max_splits = pblocks / 8 > 1 ? (pblocks / 8 < 16 ? pblocks / 8 : 16) : 1;
+  long long best_cost = -1;
+  for (int n = 1; n <= max_splits; ++n) {
+    const int sb = ((pblocks + n - 1) / n + 3) / 4 * 4;
+    const int nsplit = (pblocks + sb - 1) / sb;
+    if (nsplit != n) continue;  // the same split as a smaller count
+    const long long waves = (per_split * n + slots - 1) / slots;
+    const long long cost = waves * (sb + 8);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      pp.split_blocks = sb;
+      pp.pre_slots = n;
+    }
+  }
+  return pp;
 }
 
 using LaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const pkv::DecodeParams&, dim3, cudaStream_t,
@@ -295,7 +347,7 @@ int32_t pkv_decode_partition_tokens(int32_t batch, int32_t num_kv_heads, int32_t
 size_t pkv_decode_workspace_tickets_bytes(void) { return static_cast<size_t>(kTickets) * sizeof(int32_t); }
 
 static pkv_status plan(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_t max_len, bool fp8, Split* sp,
-                       WsLayout* ws, Variant* var, DeviceInfo** devp) {
+                       WsLayout* ws, Variant* var, DeviceInfo** devp, int pre_slots = 0) {
   if (batch < 0 || batch > 65535) return fail(PKV_ERR_INVALID_ARG, "batch must be in [0, 65535]");
   if (hkv <= 0 || hq <= 0 || hq % hkv != 0)
     return fail(PKV_ERR_INVALID_ARG, "num_q_heads (%d) must be a positive multiple of num_kv_heads (%d)", hq, hkv);
@@ -309,11 +361,34 @@ static pkv_status plan(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_
   if (st != PKV_OK) return st;
   *var = pick_variant(d, fp8, g);
   const pkv::DecodeLaunchInfo li = var->info();
-  *sp = fit_split(choose_split(batch, hkv, max_len, dev->sm_count), g, max_len, li.tile_area_bytes);
+  *sp = fit_split(choose_split(batch, hkv, max_len, dev->sm_count), g, max_len, li.tile_area_bytes, pre_slots);
   if (sp->max_splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "context too long for the partition grid");
-  *ws = ws_layout(batch, hkv, g, d, *sp);
+  if (static_cast<long long>(g) * (pre_slots + sp->max_splits + 1) * 4 > li.tile_area_bytes)
+    return fail(PKV_ERR_UNSUPPORTED, "too many partial records per sequence to merge");
+  *ws = ws_layout(batch, hkv, g, d, *sp, pre_slots);
   *devp = dev;
   return PKV_OK;
+}
+
+size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t max_context_len, int32_t num_prefixes, int32_t max_members,
+                                  int32_t max_prefix_len) {
+  t_last_error.clear();
+  if (num_prefixes < 0 || max_members < 0 || max_prefix_len < 0 || num_kv_heads <= 0 || num_q_heads <= 0) {
+    fail(PKV_ERR_INVALID_ARG, "negative prefix sizes or non-positive head counts");
+    return 0;
+  }
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != PKV_OK) return 0;
+  const PrefixPlan pp = plan_prefix(num_prefixes, max_members, max_prefix_len, num_q_heads / num_kv_heads,
+                                    num_kv_heads, dev->sm_count);
+  Split sp;
+  WsLayout ws;
+  Variant var;
+  if (plan(batch, num_q_heads, num_kv_heads, head_dim, max_context_len, false, &sp, &ws, &var, &dev,
+           pp.pre_slots) != PKV_OK)
+    return 0;
+  return ws.total;
 }
 
 size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -329,15 +404,18 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
   return ws.total;
 }
 
-pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q, const int32_t* block_tables,
-                                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
-                                      int32_t num_q_heads, int32_t max_context_len, float softmax_scale, void* out,
-                                      pkv_out_dtype out_dtype, void* workspace, size_t workspace_bytes,
-                                      pkv_stream_t stream) {
-  t_last_error.clear();
-  pkv_status st = check_cache(cache);
-  if (st != PKV_OK) return st;
-  if (batch == 0) return PKV_OK;
+}  // extern "C"
+
+namespace {
+
+// Validation and launch shared by the plain and the cascade decode: the decode kernel over
+// each sequence's own blocks, merging pre_slots shared-prefix records per (b, h) for the
+// sequences that seq_prefix marks (none when seq_prefix is NULL).
+pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                         int32_t max_context_len, float softmax_scale, void* out, pkv_out_dtype out_dtype,
+                         void* workspace, size_t workspace_bytes, pkv_stream_t stream, const int32_t* seq_prefix,
+                         int pre_slots) {
   if (!q || !block_tables || !context_lens || !out)
     return fail(PKV_ERR_INVALID_ARG, "q, block_tables, context_lens and out must be non-NULL");
   if (!aligned(q, 16)) return fail(PKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
@@ -356,7 +434,9 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q
   WsLayout ws;
   Variant var;
   DeviceInfo* dev = nullptr;
-  st = plan(batch, num_q_heads, cache->num_kv_heads, cache->head_dim, max_context_len, fp8, &sp, &ws, &var, &dev);
+  pkv_status st =
+      plan(batch, num_q_heads, cache->num_kv_heads, cache->head_dim, max_context_len, fp8, &sp, &ws, &var, &dev,
+           pre_slots);
   if (st != PKV_OK) return st;
   if (ws.total > 0) {
     if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", ws.total);
@@ -379,6 +459,7 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q
   p.tickets = ws.total ? reinterpret_cast<int32_t*>(wsb) : nullptr;
   p.part_ml = ws.total ? reinterpret_cast<float*>(wsb + ws.tickets) : nullptr;
   p.part_acc = ws.total ? reinterpret_cast<float*>(wsb + ws.tickets + ws.ml) : nullptr;
+  p.seq_prefix = pre_slots > 0 ? seq_prefix : nullptr;
   p.status = dev->status;
   p.max_blocks = max_blocks_per_seq;
   p.hq = num_q_heads;
@@ -387,6 +468,8 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q
   p.max_context_len = max_context_len;
   p.split_blocks = sp.split_blocks;
   p.max_splits = sp.max_splits;
+  p.pre_slots = pre_slots;
+  p.rec_slots = pre_slots + sp.max_splits;
   p.score_scale = softmax_scale * 1.4426950408889634f;  // log2(e)
   p.out_fp32 = out_dtype == PKV_OUT_FP32;
   int device = 0;
@@ -396,6 +479,120 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q
   cudaError_t e = var.launch(tk, tv, p, grid, reinterpret_cast<cudaStream_t>(stream), device);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q, const int32_t* block_tables,
+                                      int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                                      int32_t num_q_heads, int32_t max_context_len, float softmax_scale, void* out,
+                                      pkv_out_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                      pkv_stream_t stream) {
+  t_last_error.clear();
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (batch == 0) return PKV_OK;
+  return decode_common(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, max_context_len,
+                       softmax_scale, out, out_dtype, workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void* q, const pkv_prefix_desc* px,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
+                                        int32_t max_context_len, float softmax_scale, void* out,
+                                        pkv_out_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                        pkv_stream_t stream) {
+  t_last_error.clear();
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (!px) return fail(PKV_ERR_INVALID_ARG, "prefixes must be non-NULL");
+  if (px->num_prefixes < 0 || px->max_members < 0 || px->max_prefix_len < 0 || px->max_prefix_blocks < 0)
+    return fail(PKV_ERR_INVALID_ARG, "prefix sizes must be non-negative");
+  if (batch == 0) return PKV_OK;
+  if (batch < 0) return fail(PKV_ERR_INVALID_ARG, "batch must be >= 0");
+  const bool any_prefix = px->num_prefixes > 0 && px->max_members > 0 && px->max_prefix_len > 0;
+  if (!any_prefix)
+    return decode_common(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                         max_context_len, softmax_scale, out, out_dtype, workspace, workspace_bytes, stream, nullptr,
+                         0);
+  if (!px->prefix_tables || !px->prefix_lens || !px->member_indptr || !px->member_seqs || !px->seq_prefix)
+    return fail(PKV_ERR_INVALID_ARG, "prefix tables, lengths, member lists and seq_prefix must be non-NULL");
+  if (!aligned(px->prefix_tables, 4) || !aligned(px->prefix_lens, 4) || !aligned(px->member_indptr, 4) ||
+      !aligned(px->member_seqs, 4) || !aligned(px->seq_prefix, 4))
+    return fail(PKV_ERR_INVALID_ARG, "prefix arrays must be 4-byte aligned");
+  if (px->max_prefix_len % 16 != 0) return fail(PKV_ERR_INVALID_ARG, "max_prefix_len must be a multiple of 16");
+  if (static_cast<int64_t>(px->max_prefix_blocks) * 16 < px->max_prefix_len)
+    return fail(PKV_ERR_INVALID_ARG, "max_prefix_len exceeds max_prefix_blocks * 16");
+  const int hkv = cache->num_kv_heads;
+  if (num_q_heads <= 0 || num_q_heads % hkv != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads must be a positive multiple of num_kv_heads");
+  const int g = num_q_heads / hkv;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  const PrefixPlan pp = plan_prefix(px->num_prefixes, px->max_members, px->max_prefix_len, g, hkv, dev->sm_count);
+  if (static_cast<long long>(px->num_prefixes) * pp.pre_slots > 65535 || pp.tiles > 0x7fffffff / 2)
+    return fail(PKV_ERR_UNSUPPORTED, "too many prefixes for the prefix-pass grid");
+  Split sp;
+  WsLayout ws;
+  Variant var;
+  if ((st = plan(batch, num_q_heads, hkv, cache->head_dim, max_context_len, false, &sp, &ws, &var, &dev,
+                 pp.pre_slots)) != PKV_OK)
+    return st;
+  if (!workspace) return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes required", ws.total);
+  if (!aligned(workspace, 256)) return fail(PKV_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (workspace_bytes < ws.total)
+    return fail(PKV_ERR_WORKSPACE, "workspace has %zu bytes, %zu required", workspace_bytes, ws.total);
+  if (!q || !aligned(q, 16)) return fail(PKV_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
+  if (!std::isfinite(softmax_scale)) return fail(PKV_ERR_INVALID_ARG, "softmax_scale must be finite");
+
+  const bool fp8 = cache->kv_dtype == PKV_KV_FP8_E4M3;
+  CUtensorMap tk, tv;
+  const bool maps_ok =
+      fp8 ? encode_kv_map(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim, true) &&
+                encode_kv_map(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim, true)
+          : encode_kv_map_sw128(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim) &&
+                encode_kv_map_sw128(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim);
+  if (!maps_ok) return fail(PKV_ERR_INVALID_ARG, "cannot describe the KV pool as a TMA tensor map");
+  pkv::PrefixParams pr{};
+  pr.q = static_cast<const uint16_t*>(q);
+  pr.prefix_tables = px->prefix_tables;
+  pr.prefix_lens = px->prefix_lens;
+  pr.indptr = px->member_indptr;
+  pr.seqs = px->member_seqs;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  pr.part_ml = reinterpret_cast<float*>(wsb + ws.tickets);
+  pr.part_acc = reinterpret_cast<float*>(wsb + ws.tickets + ws.ml);
+  pr.status = dev->status;
+  pr.max_prefix_blocks = px->max_prefix_blocks;
+  pr.max_members = px->max_members;
+  pr.batch = batch;
+  pr.hq = num_q_heads;
+  pr.hkv = hkv;
+  pr.group = g;
+  pr.num_blocks = static_cast<int>(cache->num_blocks);
+  pr.split_blocks = pp.split_blocks;
+  pr.pre_slots = pp.pre_slots;
+  pr.rec_slots = pp.pre_slots + sp.max_splits;
+  pr.score_scale = softmax_scale * 1.4426950408889634f;  // log2(e)
+  pr.scales = cache->scales;
+  int device = 0;
+  cudaGetDevice(&device);
+  const dim3 pgrid(static_cast<unsigned>(pp.tiles), static_cast<unsigned>(hkv),
+                   static_cast<unsigned>(px->num_prefixes * pp.pre_slots));
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (cache->head_dim == 64)
+    e = fp8 ? pkv::launch_cascade_prefix<64, true>(tk, tv, pr, pgrid, cs, device)
+            : pkv::launch_cascade_prefix<64, false>(tk, tv, pr, pgrid, cs, device);
+  else
+    e = fp8 ? pkv::launch_cascade_prefix<128, true>(tk, tv, pr, pgrid, cs, device)
+            : pkv::launch_cascade_prefix<128, false>(tk, tv, pr, pgrid, cs, device);
+  if (e != cudaSuccess) return cuda_fail(e, "prefix-pass launch");
+  return decode_common(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, max_context_len,
+                       softmax_scale, out, out_dtype, workspace, workspace_bytes, stream, px->seq_prefix,
+                       pp.pre_slots);
 }
 
 pkv_status pkv_check_device_status(pkv_stream_t stream, uint32_t* flags) {

@@ -1,0 +1,169 @@
+"""Cascade (two-level) decode on the GPU: shared prefixes attended once for all their
+members on the tensor cores, each sequence's own blocks by the decode kernel, merged with
+log-sum-exp weights.  The reference is the oracle's plain decode over each sequence's
+whole table (prefix blocks, then its own): the split is exact (habr.com/ru/articles/1021832,
+section 3), so the two must agree within the bf16 tolerance -- the prefix pass rounds the
+softmax weights to bf16 for its tensor-core P V product."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_helpers import assert_close, oracle_pools_after_append, split_tokens, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_kv_cache_17_gb300 as m
+
+    m.check_device_status()
+    return m
+
+
+def run_cascade(pkv, q, kd, vd, c: W.CascadeInputs, scale, out_dtype=torch.float32):
+    dev = q.device
+    out = torch.empty(q.shape, dtype=out_dtype, device=dev)
+    pkv.cascade_decode_attention(q, kd, vd, c.prefix_tables.to(dev), c.prefix_lens.to(dev), c.member_indptr.to(dev),
+                                 c.member_seqs.to(dev), c.seq_prefix.to(dev), c.block_tables.to(dev),
+                                 c.context_lens.to(dev), scale, out, max_members=c.max_members,
+                                 max_prefix_len=c.max_prefix_len,
+                                 max_context_len=max(16, int(c.context_lens.max())))
+    torch.cuda.synchronize()
+    return out
+
+
+def test_prefix_shared_workload(pkv):
+    w = W.make_workload("prefix_shared")
+    t = to_dev(w)
+    pkv.paged_kv_append(t["k_new"], t["v_new"], t["slot_mapping"], t["k_cache"], t["v_cache"])
+    c = w.cascade()
+    out = run_cascade(pkv, t["q"], t["k_cache"], t["v_cache"], c, w.cfg.softmax_scale)
+    assert pkv.check_device_status() == 0
+    a, kc, vc = oracle_pools_after_append(w)
+    pairs = W.sample_pairs(w, 48, seed=3)
+    ref = oracle.decode_pairs(a["q"], kc, vc, oracle.KV_BF16, a["block_tables"], a["context_lens"],
+                              w.cfg.softmax_scale, pairs, nthreads=8)
+    got = out.cpu().double().numpy()[pairs[:, 0], pairs[:, 1]]
+    assert_close(got, ref, "bf16", "cascade prefix_shared")
+    # and the plain decode over the whole tables gives the same answer within tolerance
+    plain = torch.empty_like(out)
+    pkv.paged_decode_attention(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"],
+                               w.cfg.softmax_scale, plain, max_context_len=int(w.context_lens.max()))
+    torch.cuda.synchronize()
+    assert_close(got, plain.cpu().double().numpy()[pairs[:, 0], pairs[:, 1]], "bf16", "cascade vs plain decode")
+
+
+def build_case(hkv, g, d, seed):
+    """Seven sequences over a 96-block pool: prefix A (3 blocks: a partial 64-key stage) for
+    sequences 0, 2, 5; prefix B (9 blocks) for 1, 3, 6; sequence 4 has none; sequence 5's
+    own part is empty; sequence 6 owns one partial block."""
+    nb = 96
+    gen = torch.Generator().manual_seed(seed)
+    pool = W.BlockPool(nb, generator=gen)
+    pa, pb = pool.allocate(3), pool.allocate(9)
+    own = {0: 37, 1: 100, 2: 16, 3: 250, 4: 77, 5: 0, 6: 5}
+    seqs = []
+    for b in range(7):
+        pre = pa if b in (0, 2, 5) else (pb if b in (1, 3, 6) else [])
+        blocks = list(pre) + pool.allocate(W.blocks_for_tokens(own[b]))
+        seqs.append(W.Sequence_(len(pre) * 16 + own[b], blocks))
+    c = W.cascade_split(seqs, [[0, 2, 5], [1, 3, 6]], [3, 9])
+    hq = hkv * g
+    kp = W.randn_bf16((nb, 16, hkv, d), seed, "k_pool")
+    vp = W.randn_bf16((nb, 16, hkv, d), seed, "v_pool")
+    q = W.randn_bf16((7, hq, d), seed, "q")
+    full = torch.zeros((7, max(len(s.blocks) for s in seqs)), dtype=torch.int32)
+    for b, s in enumerate(seqs):
+        full[b, : len(s.blocks)] = torch.tensor(s.blocks, dtype=torch.int32)
+    lens = torch.tensor([s.length for s in seqs], dtype=torch.int32)
+    return c, kp, vp, q, full, lens
+
+
+@pytest.mark.parametrize("hkv,g,d", [(2, 4, 128), (1, 8, 128), (4, 1, 64), (2, 2, 64), (3, 8, 64)])
+def test_edge_cases(pkv, hkv, g, d):
+    c, kp, vp, q, full, lens = build_case(hkv, g, d, seed=11 + g + d)
+    scale = d ** -0.5
+    out = run_cascade(pkv, q.cuda(), kp.cuda(), vp.cuda(), c, scale)
+    assert pkv.check_device_status() == 0
+    ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
+                            lens.numpy(), scale)
+    assert_close(out.cpu().double().numpy(), ref, "bf16", f"cascade edges hkv={hkv} g={g} d={d}")
+
+
+@pytest.mark.parametrize("split", [16, 64])
+def test_split_suffixes_merge_with_prefix(pkv, split):
+    c, kp, vp, q, full, lens = build_case(2, 4, 128, seed=5)
+    with split_tokens(split):
+        out = run_cascade(pkv, q.cuda(), kp.cuda(), vp.cuda(), c, 0.1, out_dtype=torch.bfloat16)
+    assert pkv.check_device_status() == 0
+    ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
+                            lens.numpy(), 0.1)
+    assert_close(out.cpu().double().numpy(), ref, "bf16", f"cascade split {split}")
+
+
+def test_no_prefixes_is_plain_decode(pkv):
+    w = W.make_workload("tiny")
+    t = to_dev(w)
+    c = w.cascade()
+    assert c.prefix_tables.shape[0] == 0
+    out = run_cascade(pkv, t["q"], t["k_cache"], t["v_cache"], c, w.cfg.softmax_scale)
+    plain = torch.empty_like(out)
+    pkv.paged_decode_attention(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"],
+                               w.cfg.softmax_scale, plain)
+    torch.cuda.synchronize()
+    assert torch.equal(out, plain)
+
+
+def test_fp8_fork_workload(pkv):
+    w = W.make_workload("fp8_fork")
+    t = to_dev(w)
+    pkv.paged_kv_append(t["k_new"], t["v_new"], t["slot_mapping"], t["k_cache"], t["v_cache"], scales=t["scales"])
+    c = w.cascade()
+    dev = t["q"].device
+    out = torch.empty(t["q"].shape, dtype=torch.float32, device=dev)
+    pkv.cascade_decode_attention(t["q"], t["k_cache"], t["v_cache"], c.prefix_tables.to(dev), c.prefix_lens.to(dev),
+                                 c.member_indptr.to(dev), c.member_seqs.to(dev), c.seq_prefix.to(dev),
+                                 c.block_tables.to(dev), c.context_lens.to(dev), w.cfg.softmax_scale, out,
+                                 max_members=c.max_members, max_prefix_len=c.max_prefix_len,
+                                 max_context_len=max(16, int(c.context_lens.max())), scales=t["scales"])
+    torch.cuda.synchronize()
+    assert pkv.check_device_status() == 0
+    a, kc, vc = oracle_pools_after_append(w)
+    pairs = W.sample_pairs(w, 48, seed=4)
+    ref = oracle.decode_pairs(a["q"], kc, vc, oracle.KV_E4M3, a["block_tables"], a["context_lens"],
+                              w.cfg.softmax_scale, pairs, scales=a["scales"], nthreads=8)
+    got = out.cpu().double().numpy()[pairs[:, 0], pairs[:, 1]]
+    assert_close(got, ref, "fp8", "cascade fp8_fork")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fp8_edge_cases(pkv, d):
+    c, kp, vp, q, full, lens = build_case(2, 4, d, seed=7 + d)
+    # quantise the pool with per-head scales (the harness's rule: max |x| -> 448)
+    def quant(x):
+        sc = (x.float().abs().amax(dim=(0, 1, 3)) / 448.0).to(torch.float32)
+        return (x.float() / sc.view(1, 1, -1, 1)).to(torch.float8_e4m3fn).view(torch.uint8), sc
+    k8, ks = quant(kp)
+    v8, vs = quant(vp)
+    scales = torch.stack([ks, vs]).contiguous()
+    scale = d ** -0.5
+    dev = "cuda"
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    pkv.cascade_decode_attention(q.cuda(), k8.cuda(), v8.cuda(), c.prefix_tables.cuda(), c.prefix_lens.cuda(),
+                                 c.member_indptr.cuda(), c.member_seqs.cuda(), c.seq_prefix.cuda(),
+                                 c.block_tables.cuda(), c.context_lens.cuda(), scale, out, max_members=c.max_members,
+                                 max_prefix_len=c.max_prefix_len, max_context_len=max(16, int(c.context_lens.max())),
+                                 scales=scales.cuda())
+    torch.cuda.synchronize()
+    assert pkv.check_device_status() == 0
+    ref = oracle.decode_all(W.bf16_bits(q), k8.numpy(), v8.numpy(), oracle.KV_E4M3, full.numpy(), lens.numpy(),
+                            scale, scales=scales.numpy())
+    assert_close(out.cpu().double().numpy(), ref, "fp8", f"cascade fp8 edges d={d}")

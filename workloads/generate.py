@@ -104,6 +104,20 @@ class Workload:
     def total_tokens(self) -> int:
         return sum(s.length for s in self.seqs)
 
+    def cascade(self) -> CascadeInputs:
+        """This step's shared prefixes (the shared-prefix and fork workloads) as cascade
+        inputs; other workloads have none."""
+        c = self.cfg
+        B = self.batch
+        if c.kind == "prefix":
+            groups, pblk = [list(range(B))], [c.prefix_len // BLOCK_SIZE]
+        elif c.kind == "fork":
+            groups = [list(range(i * c.samples, (i + 1) * c.samples)) for i in range(c.prompts)]
+            pblk = [c.prefix_len // BLOCK_SIZE] * c.prompts
+        else:
+            groups, pblk = [], []
+        return cascade_split(self.seqs, groups, pblk)
+
     def np(self) -> Dict[str, np.ndarray]:
         """numpy views for the oracle (bf16 as uint16 bits, e4m3 as uint8 codes)."""
         def pool(t):
@@ -119,6 +133,59 @@ class Workload:
             "context_lens": self.context_lens.numpy(),
             "scales": None if self.scales is None else self.scales.numpy(),
         }
+
+
+@dataclass
+class CascadeInputs:
+    """The same decode step split into shared prefixes and per-sequence suffixes."""
+
+    prefix_tables: torch.Tensor  # [P, max_prefix_blocks] int32
+    prefix_lens: torch.Tensor    # [P] int32 (multiples of 16)
+    member_indptr: torch.Tensor  # [P + 1] int32
+    member_seqs: torch.Tensor    # [members] int32
+    seq_prefix: torch.Tensor     # [B] int32, -1 without a prefix
+    block_tables: torch.Tensor   # [B, max_suffix_blocks] int32: blocks after the prefix
+    context_lens: torch.Tensor   # [B] int32: tokens after the prefix
+    max_members: int
+    max_prefix_len: int
+
+
+def cascade_split(seqs: List[Sequence_], groups: List[List[int]], prefix_blocks: List[int]) -> CascadeInputs:
+    """Cascade inputs for sequences where group i (sequence indices) shares its first
+    prefix_blocks[i] blocks (the same physical ids in every member).  Sequences in no group
+    keep their whole table."""
+    B = len(seqs)
+    P = len(groups)
+    seq_prefix = [-1] * B
+    for i, grp in enumerate(groups):
+        for b in grp:
+            assert seq_prefix[b] == -1, "a sequence belongs to at most one prefix"
+            assert seqs[b].blocks[: prefix_blocks[i]] == seqs[grp[0]].blocks[: prefix_blocks[i]]
+            assert seqs[b].length >= prefix_blocks[i] * BLOCK_SIZE
+            seq_prefix[b] = i
+    mpb = max([1] + list(prefix_blocks))
+    ptab = torch.zeros((max(P, 0), mpb), dtype=torch.int32)
+    for i, grp in enumerate(groups):
+        ptab[i, : prefix_blocks[i]] = torch.tensor(seqs[grp[0]].blocks[: prefix_blocks[i]], dtype=torch.int32)
+    suffix = []
+    for b, sq in enumerate(seqs):
+        nb = prefix_blocks[seq_prefix[b]] if seq_prefix[b] >= 0 else 0
+        suffix.append((sq.blocks[nb:], sq.length - nb * BLOCK_SIZE))
+    msb = max([1] + [len(bl) for bl, _ in suffix])
+    stab = torch.zeros((B, msb), dtype=torch.int32)
+    for b, (bl, _) in enumerate(suffix):
+        if bl:
+            stab[b, : len(bl)] = torch.tensor(bl, dtype=torch.int32)
+    indptr = [0]
+    for grp in groups:
+        indptr.append(indptr[-1] + len(grp))
+    return CascadeInputs(
+        prefix_tables=ptab, prefix_lens=torch.tensor([n * BLOCK_SIZE for n in prefix_blocks], dtype=torch.int32),
+        member_indptr=torch.tensor(indptr, dtype=torch.int32),
+        member_seqs=torch.tensor([b for grp in groups for b in grp], dtype=torch.int32),
+        seq_prefix=torch.tensor(seq_prefix, dtype=torch.int32), block_tables=stab,
+        context_lens=torch.tensor([n for _, n in suffix], dtype=torch.int32),
+        max_members=max([0] + [len(grp) for grp in groups]), max_prefix_len=max([0] + list(prefix_blocks)) * BLOCK_SIZE)
 
 
 def _lengths(cfg: Config, g: torch.Generator) -> List[int]:
