@@ -1,8 +1,8 @@
-// Instantiations of the paged decode kernel for a bf16 KV pool (head_dim 64 / 128,
-// query-group sizes 1, 2, 4, 8).
+// Instantiations of the paged decode kernel for a bf16 KV pool (plain decode),
+// head_dim 64 / 128, query-group sizes 1, 2, 4, 8.
 #include "decode_launch.cuh"
 
 namespace pkv {
-PKV_FOR_EACH_GROUP(PKV_DEFINE_DECODE, 64, false)
-PKV_FOR_EACH_GROUP(PKV_DEFINE_DECODE, 128, false)
+PKV_FOR_EACH_GROUP(PKV_DEFINE_DECODE, 64, false, false)
+PKV_FOR_EACH_GROUP(PKV_DEFINE_DECODE, 128, false, false)
 }  // namespace pkv

@@ -292,7 +292,9 @@ __device__ __forceinline__ void merge_records(const DecodeParams& p, int b, int 
   }
 }
 
-template <int D, int G, bool FP8, int NWC, int STAGES>
+// CAS: the cascade variant, which merges shared-prefix records (seq_prefix, pre_slots);
+// the plain variant carries none of that code.
+template <int D, int G, bool FP8, int NWC, int STAGES, bool CAS>
 __global__ void __launch_bounds__((NWC + 1) * 32)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeParams p) {
@@ -318,8 +320,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   // call the preceding kernel is the prefix pass, which lets this grid start once all its
   // CTAs are past their own wait (so the append's results are visible); this kernel then
   // waits for the prefix pass itself only before it reads the prefix records.
-  const bool cascade = p.seq_prefix != nullptr;
-  if (!cascade) pdl_wait();
+  if constexpr (!CAS) pdl_wait();
 
   // ---- sequence length (checked, clamped) and this CTA's share of it
   int len = p.context_lens[b];
@@ -335,10 +336,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   const int hq0 = h * G;
 
   // shared-prefix records (written by the prefix pass) come first among this (b, h)'s records
-  const int npre = (p.seq_prefix != nullptr && p.seq_prefix[b] >= 0) ? p.pre_slots : 0;
+  int npre = 0;
+  if constexpr (CAS) npre = p.seq_prefix[b] >= 0 ? p.pre_slots : 0;
   if (nblk == 0) {  // no own blocks: partition 0 writes zeros, or the prefix result alone
     if (s == 0) {
-      if (npre > 0) {
+      if (CAS && npre > 0) {
         pdl_wait();
         merge_records<D, G, FP8>(p, b, h, 0, npre, reinterpret_cast<float*>(smem), C::kThreads);
       } else {
@@ -505,7 +507,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   if constexpr (FP8) vfix = p.scales[p.hkv + h];
   const bool single = (nsplit == 1 && npre == 0);
   // one partition and prefix records: merge them right here (no record, no ticket)
-  const bool with_prefix = (nsplit == 1 && npre > 0);
+  const bool with_prefix = CAS && (nsplit == 1 && npre > 0);
   if (with_prefix) pdl_wait();
   const size_t prec0 = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots;
   for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
@@ -522,7 +524,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       num = fmaf(wt, aw[(w * GW + gw) * D + d], num);
       den = fmaf(wt, lw[w * GW + gw], den);
     }
-    if (with_prefix) {
+    if (CAS && with_prefix) {
       // combine with the prefix records in record order: theirs, then this partition's
       float Mt = M;
       for (int j = 0; j < npre; ++j) Mt = fmaxf(Mt, __ldcg(&p.part_ml[((prec0 + j) * G + g) * 2]));
@@ -549,7 +551,8 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
       else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
     } else {
-      const size_t rec = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots + p.pre_slots + s;
+      const size_t rec = CAS ? (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots + p.pre_slots + s
+                             : (static_cast<size_t>(b) * p.hkv + h) * p.max_splits + s;
       p.part_acc[(rec * G + g) * D + d] = num;
       if (d == 0) {
         p.part_ml[(rec * G + g) * 2 + 0] = M;
@@ -570,10 +573,44 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  if (npre > 0) pdl_wait();
-  // this sequence's records: the prefix pass's (if any), then one per partition
-  merge_records<D, G, FP8>(p, b, h, p.pre_slots - npre, p.pre_slots + nsplit, reinterpret_cast<float*>(smem),
-                           C::kThreads);
+  if constexpr (CAS) {
+    if (npre > 0) pdl_wait();
+    // this sequence's records: the prefix pass's (if any), then one per partition
+    merge_records<D, G, FP8>(p, b, h, p.pre_slots - npre, p.pre_slots + nsplit, reinterpret_cast<float*>(smem),
+                             C::kThreads);
+  } else {
+    // weights per (g, partition) in the tile area: w[g][s] = 2^(m_s - M_g) / sum_s 2^(m_s - M_g) l_s
+    float* wts = reinterpret_cast<float*>(smem);
+    const size_t rec0 = (static_cast<size_t>(b) * p.hkv + h) * p.max_splits;
+    for (int g = warp; g < G; g += NWC + 1) {
+      float M = -INFINITY;
+      for (int j = lane; j < nsplit; j += 32) M = fmaxf(M, __ldcg(&p.part_ml[((rec0 + j) * G + g) * 2]));
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, shfl_xor(M, m));
+      // the denominator is summed in partition order by lane 0 (deterministic)
+      for (int j = lane; j < nsplit; j += 32)
+        wts[g * p.max_splits + j] = fast_exp2(__ldcg(&p.part_ml[((rec0 + j) * G + g) * 2]) - M);
+      __syncwarp();
+      if (lane == 0) {
+        float den = 0.f;
+        for (int j = 0; j < nsplit; ++j)
+          den = fmaf(wts[g * p.max_splits + j], __ldcg(&p.part_ml[((rec0 + j) * G + g) * 2 + 1]), den);
+        wts[G * p.max_splits + g] = 1.0f / den;
+      }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
+      const int g = e / D, d = e % D;
+      float num = 0.f;
+      for (int j = 0; j < nsplit; ++j)
+        num = fmaf(wts[g * p.max_splits + j], __ldcg(&p.part_acc[((rec0 + j) * G + g) * D + d]), num);
+      float o = num * wts[G * p.max_splits + g];
+      if constexpr (FP8) o = (o * 1152921504606846976.0f) * (vfix * 1152921504606846976.0f);
+      const size_t oi = (out_row0 + g) * D + d;
+      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
+      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+    }
+  }
   if (threadIdx.x == 0) p.tickets[b * p.hkv + h] = 0;  // leave the ticket region zero
 }
 

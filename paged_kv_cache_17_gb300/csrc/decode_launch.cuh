@@ -24,19 +24,19 @@ struct DecodeLaunchInfo {
   int tile_area_bytes;  // bytes usable by the cross-partition merge weights
 };
 
-template <int D, int G, bool FP8>
+template <int D, int G, bool FP8, bool CAS>
 DecodeLaunchInfo decode_launch_info() {
   using S = DecodeShape<D, FP8>;
   using C = DecodeCfg<D, G, FP8, S::kNWC, S::kStages>;
   return DecodeLaunchInfo{C::kThreads, C::kSmemBytes, C::kTilesBytes};
 }
 
-template <int D, int G, bool FP8>
+template <int D, int G, bool FP8, bool CAS>
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, dim3 grid,
                           cudaStream_t stream, int device) {
   using S = DecodeShape<D, FP8>;
   using C = DecodeCfg<D, G, FP8, S::kNWC, S::kStages>;
-  auto kern = paged_decode_kernel<D, G, FP8, S::kNWC, S::kStages>;
+  auto kern = paged_decode_kernel<D, G, FP8, S::kNWC, S::kStages, CAS>;
   static bool configured[64] = {};
   if (device >= 0 && device < 64 && !configured[device]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -56,22 +56,27 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-// Explicit instantiations live in decode_bf16.cu / decode_e4m3.cu.
-#define PKV_DECLARE_DECODE(D, G, FP8)                                                                  \
-  extern template DecodeLaunchInfo decode_launch_info<D, G, FP8>();                                    \
-  extern template cudaError_t launch_decode<D, G, FP8>(const CUtensorMap&, const CUtensorMap&,        \
-                                                       const DecodeParams&, dim3, cudaStream_t, int);
-#define PKV_DEFINE_DECODE(D, G, FP8)                                                             \
-  template DecodeLaunchInfo decode_launch_info<D, G, FP8>();                                     \
-  template cudaError_t launch_decode<D, G, FP8>(const CUtensorMap&, const CUtensorMap&,         \
-                                                const DecodeParams&, dim3, cudaStream_t, int);
+// Explicit instantiations live in decode_bf16.cu / decode_e4m3.cu (plain) and
+// cascade_bf16.cu / cascade_e4m3.cu (cascade variants).
+#define PKV_DECLARE_DECODE(D, G, FP8, CAS)                                                              \
+  extern template DecodeLaunchInfo decode_launch_info<D, G, FP8, CAS>();                                \
+  extern template cudaError_t launch_decode<D, G, FP8, CAS>(const CUtensorMap&, const CUtensorMap&,    \
+                                                            const DecodeParams&, dim3, cudaStream_t, int);
+#define PKV_DEFINE_DECODE(D, G, FP8, CAS)                                                        \
+  template DecodeLaunchInfo decode_launch_info<D, G, FP8, CAS>();                                \
+  template cudaError_t launch_decode<D, G, FP8, CAS>(const CUtensorMap&, const CUtensorMap&,    \
+                                                     const DecodeParams&, dim3, cudaStream_t, int);
 
-#define PKV_FOR_EACH_GROUP(M, D, FP8) M(D, 1, FP8) M(D, 2, FP8) M(D, 4, FP8) M(D, 8, FP8)
+#define PKV_FOR_EACH_GROUP(M, D, FP8, CAS) M(D, 1, FP8, CAS) M(D, 2, FP8, CAS) M(D, 4, FP8, CAS) M(D, 8, FP8, CAS)
 
-PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, false)
-PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, false)
-PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, true)
-PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, true)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, false, false)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, false, false)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, true, false)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, true, false)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, false, true)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, false, true)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, true, true)
+PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, true, true)
 
 // copy-on-write block copy (copy_blocks.cu)
 cudaError_t launch_copy_blocks(const int64_t* pairs, int64_t num_pairs, int64_t block_bytes, void* k_cache,

@@ -253,20 +253,25 @@ struct Variant {
   InfoFn info;
 };
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool CAS>
 Variant pick_g(int g) {
   switch (g) {
-    case 1: return {pkv::launch_decode<D, 1, FP8>, pkv::decode_launch_info<D, 1, FP8>};
-    case 2: return {pkv::launch_decode<D, 2, FP8>, pkv::decode_launch_info<D, 2, FP8>};
-    case 4: return {pkv::launch_decode<D, 4, FP8>, pkv::decode_launch_info<D, 4, FP8>};
-    case 8: return {pkv::launch_decode<D, 8, FP8>, pkv::decode_launch_info<D, 8, FP8>};
+    case 1: return {pkv::launch_decode<D, 1, FP8, CAS>, pkv::decode_launch_info<D, 1, FP8, CAS>};
+    case 2: return {pkv::launch_decode<D, 2, FP8, CAS>, pkv::decode_launch_info<D, 2, FP8, CAS>};
+    case 4: return {pkv::launch_decode<D, 4, FP8, CAS>, pkv::decode_launch_info<D, 4, FP8, CAS>};
+    case 8: return {pkv::launch_decode<D, 8, FP8, CAS>, pkv::decode_launch_info<D, 8, FP8, CAS>};
     default: return {nullptr, nullptr};
   }
 }
 
-Variant pick_variant(int d, bool fp8, int g) {
-  if (d == 64) return fp8 ? pick_g<64, true>(g) : pick_g<64, false>(g);
-  return fp8 ? pick_g<128, true>(g) : pick_g<128, false>(g);
+// The plain decode, or the cascade variant that merges shared-prefix records.
+Variant pick_variant(int d, bool fp8, int g, bool cas) {
+  if (cas) {
+    if (d == 64) return fp8 ? pick_g<64, true, true>(g) : pick_g<64, false, true>(g);
+    return fp8 ? pick_g<128, true, true>(g) : pick_g<128, false, true>(g);
+  }
+  if (d == 64) return fp8 ? pick_g<64, true, false>(g) : pick_g<64, false, false>(g);
+  return fp8 ? pick_g<128, true, false>(g) : pick_g<128, false, false>(g);
 }
 
 }  // namespace
@@ -359,7 +364,7 @@ static pkv_status plan(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_
   DeviceInfo* dev = nullptr;
   pkv_status st = device_info(&dev);
   if (st != PKV_OK) return st;
-  *var = pick_variant(d, fp8, g);
+  *var = pick_variant(d, fp8, g, pre_slots > 0);
   const pkv::DecodeLaunchInfo li = var->info();
   *sp = fit_split(choose_split(batch, hkv, max_len, dev->sm_count), g, max_len, li.tile_area_bytes, pre_slots);
   if (sp->max_splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "context too long for the partition grid");
