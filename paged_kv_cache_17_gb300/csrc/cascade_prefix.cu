@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include "cascade.cuh"
+#include "mma_ops.cuh"
 #include "pkv_device.cuh"
 
 namespace pkv {
@@ -41,70 +42,11 @@ constexpr int kStageKeys = kStageBlocks * kBlockSize;  // 64
 constexpr int kStages = 3;
 constexpr int kBoxBytes = kBlockSize * 128;           // one 16 x 64 bf16 box, swizzled
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-
-// D (16x8, f32) += A (16x16, bf16, row) * B (16x8, bf16, col)
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-template <bool F16>
-__device__ __forceinline__ void mma16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                      uint32_t b1) {
-  if constexpr (F16) mma_f16(d, a0, a1, a2, a3, b0, b1);
-  else mma_bf16(d, a0, a1, a2, a3, b0, b1);
-}
-
-__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
-// two E4M3 codes (low byte = first element) -> two fp16 values, exactly
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 // Shared address of key row kr (0..63 of a stage) and 16-byte chunk c (8 elements of the
-// head dim) in a stage laid out as [block][half][16 rows][128 B], 128-byte swizzled: the
-// chunk index within a 128-byte row is xor-ed with the row index mod 8.
+// head dim) in a stage laid out as [block][half][16 rows][128 B], 128-byte swizzled.
 template <int D>
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int kr, int c) {
-  constexpr int kHalves = D / 64;
-  const int box = (kr >> 4) * kHalves + (c >> 3);
-  const int r = kr & 15;
-  return base + box * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+  return swz_addr<D>(base, kr, c);
 }
 
 }  // namespace

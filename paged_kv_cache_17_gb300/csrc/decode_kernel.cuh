@@ -351,9 +351,13 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         }
       }
     }
+    if constexpr (CAS) pdl_wait();
     return;
   }
-  if (s >= nsplit) return;
+  if (s >= nsplit) {
+    if constexpr (CAS) pdl_wait();
+    return;
+  }
   const int blk0 = s * p.split_blocks;
   const int nloc = min(nblk, blk0 + p.split_blocks) - blk0;
 
@@ -560,58 +564,10 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       }
     }
   }
-  if (single || with_prefix) return;
-
-  // ================================================================ cross-partition merge
-  __shared__ int s_last;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int prev = atomicAdd(&p.tickets[b * p.hkv + h], 1);
-    s_last = (prev == nsplit - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if constexpr (CAS) {
-    if (npre > 0) pdl_wait();
-    // this sequence's records: the prefix pass's (if any), then one per partition
-    merge_records<D, G, FP8>(p, b, h, p.pre_slots - npre, p.pre_slots + nsplit, reinterpret_cast<float*>(smem),
-                             C::kThreads);
-  } else {
-    // weights per (g, partition) in the tile area: w[g][s] = 2^(m_s - M_g) / sum_s 2^(m_s - M_g) l_s
-    float* wts = reinterpret_cast<float*>(smem);
-    const size_t rec0 = (static_cast<size_t>(b) * p.hkv + h) * p.max_splits;
-    for (int g = warp; g < G; g += NWC + 1) {
-      float M = -INFINITY;
-      for (int j = lane; j < nsplit; j += 32) M = fmaxf(M, __ldcg(&p.part_ml[((rec0 + j) * G + g) * 2]));
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, shfl_xor(M, m));
-      // the denominator is summed in partition order by lane 0 (deterministic)
-      for (int j = lane; j < nsplit; j += 32)
-        wts[g * p.max_splits + j] = fast_exp2(__ldcg(&p.part_ml[((rec0 + j) * G + g) * 2]) - M);
-      __syncwarp();
-      if (lane == 0) {
-        float den = 0.f;
-        for (int j = 0; j < nsplit; ++j)
-          den = fmaf(wts[g * p.max_splits + j], __ldcg(&p.part_ml[((rec0 + j) * G + g) * 2 + 1]), den);
-        wts[G * p.max_splits + g] = 1.0f / den;
-      }
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
-      const int g = e / D, d = e % D;
-      float num = 0.f;
-      for (int j = 0; j < nsplit; ++j)
-        num = fmaf(wts[g * p.max_splits + j], __ldcg(&p.part_acc[((rec0 + j) * G + g) * D + d]), num);
-      float o = num * wts[G * p.max_splits + g];
-      if constexpr (FP8) o = (o * 1152921504606846976.0f) * (vfix * 1152921504606846976.0f);
-      const size_t oi = (out_row0 + g) * D + d;
-      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
-      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-    }
-  }
-  if (threadIdx.x == 0) p.tickets[b * p.hkv + h] = 0;  // leave the ticket region zero
+  // A record was written (or, for one partition, the output): the merge kernel that
+  // follows combines the records.  A cascade grid completes only after the prefix pass,
+  // whose records the merge kernel also reads.
+  if constexpr (CAS) pdl_wait();
 }
 
 }  // namespace pkv

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "decode_kernel.cuh"
+#include "decode_mma.cuh"
 
 namespace pkv {
 
@@ -56,6 +57,54 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
+// The tensor-core form (bf16 pools): same grid, ring depth and launch; 128-byte-swizzled
+// tensor maps.
+template <int D, int G, bool CAS>
+DecodeLaunchInfo decode_mma_launch_info() {
+  using S = DecodeShape<D, false>;
+  using C = MmaCfg<D, G, S::kNWC, S::kStages>;
+  return DecodeLaunchInfo{C::kThreads, C::kSmemBytes, C::kTilesBytes};
+}
+
+template <int D, int G, bool CAS>
+cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, dim3 grid,
+                              cudaStream_t stream, int device) {
+  using S = DecodeShape<D, false>;
+  using C = MmaCfg<D, G, S::kNWC, S::kStages>;
+  auto kern = paged_decode_mma_kernel<D, G, S::kNWC, S::kStages, CAS>;
+  static bool configured[64] = {};
+  if (device >= 0 && device < 64 && !configured[device]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured[device] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+#define PKV_DECLARE_DECODE_MMA(D, G, CAS)                                                                 \
+  extern template DecodeLaunchInfo decode_mma_launch_info<D, G, CAS>();                                   \
+  extern template cudaError_t launch_decode_mma<D, G, CAS>(const CUtensorMap&, const CUtensorMap&,       \
+                                                           const DecodeParams&, dim3, cudaStream_t, int);
+#define PKV_DEFINE_DECODE_MMA(D, G, CAS)                                                           \
+  template DecodeLaunchInfo decode_mma_launch_info<D, G, CAS>();                                   \
+  template cudaError_t launch_decode_mma<D, G, CAS>(const CUtensorMap&, const CUtensorMap&,       \
+                                                    const DecodeParams&, dim3, cudaStream_t, int);
+#define PKV_FOR_EACH_GROUP_MMA(M, D, CAS) M(D, 1, CAS) M(D, 2, CAS) M(D, 4, CAS) M(D, 8, CAS)
+PKV_FOR_EACH_GROUP_MMA(PKV_DECLARE_DECODE_MMA, 64, false)
+PKV_FOR_EACH_GROUP_MMA(PKV_DECLARE_DECODE_MMA, 128, false)
+PKV_FOR_EACH_GROUP_MMA(PKV_DECLARE_DECODE_MMA, 64, true)
+PKV_FOR_EACH_GROUP_MMA(PKV_DECLARE_DECODE_MMA, 128, true)
+
 // Explicit instantiations live in decode_bf16.cu / decode_e4m3.cu (plain) and
 // cascade_bf16.cu / cascade_e4m3.cu (cascade variants).
 #define PKV_DECLARE_DECODE(D, G, FP8, CAS)                                                              \
@@ -77,6 +126,10 @@ PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, false, true)
 PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, false, true)
 PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 64, true, true)
 PKV_FOR_EACH_GROUP(PKV_DECLARE_DECODE, 128, true, true)
+
+// merge of the partition (and prefix) records into the output (merge_partitions.cu):
+// grid (kv heads, batch), launched right after the decode kernel
+cudaError_t launch_merge_partitions(int d, int g, bool fp8, const DecodeParams& p, dim3 grid, cudaStream_t stream);
 
 // copy-on-write block copy (copy_blocks.cu)
 cudaError_t launch_copy_blocks(const int64_t* pairs, int64_t num_pairs, int64_t block_bytes, void* k_cache,

@@ -1,0 +1,338 @@
+// decode_mma.cuh -- paged GQA decode attention with the per-block products on the tensor
+// cores.
+//
+// What it computes is exactly what decode_kernel.cuh computes (habr.com/ru/articles/1021832,
+// section 3: softmax(q K^T * scale) V evaluated block by block with a running max, a
+// running sum and the rescale exp(m_old - m_new); section 4: K/V in 16-token blocks found
+// through the block table), with the same grid, producer warp, TMA ring, split-K records
+// and log-sum-exp merge.  Only the per-block arithmetic differs.  On GB300 the CUDA-core
+// form of that arithmetic costs about as much time as streaming the KV for a query group
+// of 4 and 1.7 times as much for a group of 8, so the decode is not purely bandwidth bound
+// there; here each 16-token block is two small matrix products per consumer warp:
+//
+//   S^T [16 tokens x 8] = K [16 x D] . q^T [D x 8]        (the group's G <= 8 heads as N)
+//   O^T [D x 8]        += V^T [D x 16] . P^T [16 x 8]
+//
+// as mma.sync.m16n8k16 (bf16 in, fp32 accumulate): D/16 MMAs for the scores, 2 x D/16 for
+// P V.  Tokens are the M dimension, so no row of the MMA is padding for a group of 8.  K
+// and V tiles arrive by TMA as 128-byte-swizzled 64-column boxes and are read with
+// ldmatrix (V transposed); q stays in registers as B fragments; the weights P leave the S
+// accumulators through movmatrix (an 8x8 transpose inside the warp) as the B operand of
+// the second product, split into bf16 hi + lo so that P V keeps fp32-level accuracy.
+#pragma once
+
+#include "decode_kernel.cuh"
+#include "mma_ops.cuh"
+
+namespace pkv {
+
+template <int D, int G, int NWC, int STAGES>
+struct MmaCfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTileBytes = kBlockSize * D * 2;  // 16 rows x D bf16, as kHalves boxes
+  static constexpr int kKS = D / 16;                     // k-steps of the score product
+  static constexpr int kMT = D / 16;                     // m-tiles of the output product
+  static constexpr int kThreads = (NWC + 1) * 32;
+  static constexpr int kTilesBytes = 2 * STAGES * kTileBytes;
+  static constexpr int kBarOffset = kTilesBytes;
+  static constexpr int kSmemBytes = 1024 + kBarOffset + 2 * STAGES * 8;  // 1024: alignment slack
+  static constexpr int kMergeBytes = NWC * (2 * G + G * D) * 4;
+  static_assert(kMergeBytes <= kTilesBytes, "merge scratch must fit in the tile ring");
+  static_assert(G >= 1 && G <= 8, "a query group of at most 8 heads (the MMA's N)");
+  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(STAGES % NWC == 0, "each stage is always consumed by the same warp");
+  static_assert(kTileBytes % 1024 == 0, "1024-byte aligned boxes keep the swizzle aligned with the rows");
+};
+
+template <int D, int G, int NWC, int STAGES, bool CAS>
+__global__ void __launch_bounds__((NWC + 1) * 32)
+    paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                            const DecodeParams p) {
+  using C = MmaCfg<D, G, NWC, STAGES>;
+  constexpr int KS = C::kKS, MT = C::kMT;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* k_tiles = smem;
+  uint8_t* v_tiles = smem + STAGES * C::kTileBytes;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+  uint64_t* empty_bar = full_bar + STAGES;
+
+  const int h = blockIdx.x;
+  const int b = blockIdx.y;
+  const int s = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+
+  if constexpr (!CAS) pdl_wait();
+
+  int len = p.context_lens[b];
+  {
+    const int cap = min(p.max_context_len, p.max_blocks * kBlockSize);
+    if (len < 0 || len > cap) {
+      if (threadIdx.x == 0 && s == 0) set_flag(p.status, PKV_DEVFLAG_BAD_CONTEXT_LEN);
+      len = len < 0 ? 0 : cap;
+    }
+  }
+  const int nblk = (len + kBlockSize - 1) / kBlockSize;
+  const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
+  const int hq0 = h * G;
+  int npre = 0;
+  if constexpr (CAS) npre = p.seq_prefix[b] >= 0 ? p.pre_slots : 0;
+  if (nblk == 0) {  // no own blocks: partition 0 writes zeros, or the prefix result alone
+    if (s == 0) {
+      if (CAS && npre > 0) {
+        pdl_wait();
+        merge_records<D, G, false>(p, b, h, 0, npre, reinterpret_cast<float*>(smem), C::kThreads);
+      } else {
+        for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
+          const size_t o = (static_cast<size_t>(b) * p.hq + hq0) * D + e;
+          if (p.out_fp32) reinterpret_cast<float*>(p.out)[o] = 0.f;
+          else reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(0.f);
+        }
+      }
+    }
+    if constexpr (CAS) pdl_wait();
+    return;
+  }
+  if (s >= nsplit) {
+    if constexpr (CAS) pdl_wait();
+    return;
+  }
+  const int blk0 = s * p.split_blocks;
+  const int nloc = min(nblk, blk0 + p.split_blocks) - blk0;
+
+  const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk0;
+  int ids = (warp == NWC && lane < nloc) ? row[lane] : 0;
+  // q as the B operand of the score product: column n = head gid of the group (zero
+  // columns past G), k = head_dim; one pair of bf16 words per k-step
+  uint32_t qb[KS][2];
+  if (warp < NWC) {
+    const bool live = gid < G;
+    const uint32_t* qr = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(b) * p.hq + hq0 + (live ? gid : 0)) * D);
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      qb[kk][0] = live ? qr[kk * 8 + tig] : 0u;      // dims 16kk + 2tig, +1
+      qb[kk][1] = live ? qr[kk * 8 + 4 + tig] : 0u;  // dims 16kk + 8 + 2tig, +1
+    }
+  }
+  if (threadIdx.x == NWC * 32) tma_prefetch_desc(&tm_k), tma_prefetch_desc(&tm_v);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const float sscale = p.score_scale;  // log2 units
+  bool timed_out = false;
+
+  if (warp == NWC) {
+    // ================================================================ producer warp
+    int issued = 0;
+    for (int base = 0; base < nloc && !timed_out; base += 32) {
+      const int next = (base + 32 + lane < nloc) ? row[base + 32 + lane] : 0;  // prefetch
+      if ((ids < 0 || ids >= p.num_blocks) && base + lane < nloc) set_flag(p.status, PKV_DEVFLAG_BAD_BLOCK_ID);
+      const int cnt = min(32, nloc - base);
+      for (int k = 0; k < cnt; ++k) {
+        const int pb = __shfl_sync(kFull, ids, k);
+        const int it = base + k;
+        const int st = it % STAGES;
+        if (lane == 0) {
+          if (it >= STAGES && !mbar_wait(&empty_bar[st], ((it / STAGES) - 1) & 1)) {
+            set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
+            timed_out = true;
+          }
+          if (!timed_out) {
+            // an id outside the pool reads a box entirely outside the tensor: zeros
+            const int row0 = (pb >= 0 && pb < p.num_blocks) ? pb * kBlockSize : -kBlockSize;
+            mbar_arrive_expect_tx(&full_bar[st], 2 * C::kTileBytes);
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf) {
+              tma_load_3d(k_tiles + st * C::kTileBytes + hf * 2048, &tm_k, hf * 64, h, row0, &full_bar[st]);
+              tma_load_3d(v_tiles + st * C::kTileBytes + hf * 2048, &tm_v, hf * 64, h, row0, &full_bar[st]);
+            }
+          }
+        }
+        timed_out = __shfl_sync(kFull, timed_out, 0);
+        if (timed_out) break;
+        issued = it + 1;
+      }
+      ids = next;
+    }
+    if (lane == 0) {  // every issued copy must land before the CTA reuses or releases the ring
+      for (int it = max(0, issued - STAGES); it < issued; ++it)
+        if (!mbar_wait(&full_bar[it % STAGES], (it / STAGES) & 1)) {
+          set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
+          break;
+        }
+    }
+    __syncwarp();
+  }
+
+  // per thread: heads 2tig, 2tig+1 of the group (running max, this thread's share of the
+  // running sum) and O^T fragments: o[mt] = dims 16mt + gid (+8) x heads 2tig, 2tig+1
+  float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
+  float o[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+  if (warp < NWC) {
+    // ================================================================ consumer warps
+    const int mi = lane >> 3;
+    for (int it = warp; it < nloc; it += NWC) {
+      const int sg = it % STAGES;
+      if (!mbar_wait(&full_bar[sg], (it / STAGES) & 1)) {
+        if (lane == 0) set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
+        timed_out = true;
+        break;
+      }
+      const uint32_t kb = smem_u32(k_tiles + sg * C::kTileBytes);
+      const uint32_t vb = smem_u32(v_tiles + sg * C::kTileBytes);
+      const int valid = min(kBlockSize, len - (blk0 + it) * kBlockSize);  // >= 1
+
+      // ---- S^T = K q^T: rows = tokens gid, gid+8; columns = heads 2tig, 2tig+1
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(swz_addr<D>(kb, (lane & 7) + 8 * (mi & 1), 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+        mma16<false>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = gid + 8 * (e >> 1);
+        sc[e] = tok < valid ? sc[e] * sscale : -INFINITY;
+      }
+      // ---- online softmax per head: block max over the 16 tokens (lanes of equal tig)
+      float bm0 = fmaxf(sc[0], sc[2]), bm1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+      for (int m = 4; m <= 16; m <<= 1) {
+        bm0 = fmaxf(bm0, shfl_xor(bm0, m));
+        bm1 = fmaxf(bm1, shfl_xor(bm1, m));
+      }
+      const float mn0 = fmaxf(mrun[0], bm0), mn1 = fmaxf(mrun[1], bm1);
+      const bool moved = __any_sync(kFull, (mn0 > mrun[0]) || (mn1 > mrun[1]));
+      if (moved) {
+        const float al0 = fast_exp2(mrun[0] - mn0), al1 = fast_exp2(mrun[1] - mn1);  // 2^-inf = 0 at start
+        mrun[0] = mn0;
+        mrun[1] = mn1;
+        lrun[0] *= al0;
+        lrun[1] *= al1;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          o[mt][0] *= al0;
+          o[mt][1] *= al1;
+          o[mt][2] *= al0;
+          o[mt][3] *= al1;
+        }
+      }
+      const float p0 = fast_exp2(sc[0] - mrun[0]), p1 = fast_exp2(sc[1] - mrun[1]);
+      const float p2 = fast_exp2(sc[2] - mrun[0]), p3 = fast_exp2(sc[3] - mrun[1]);
+      lrun[0] += p0 + p2;
+      lrun[1] += p1 + p3;
+      // ---- P^T as the B operand: transpose (token, head-pair) fragments to (head, token-pair)
+      uint32_t h01, l01, h23, l23;
+      split16<false>(p0, p1, h01, l01);  // token gid: heads 2tig, 2tig+1
+      split16<false>(p2, p3, h23, l23);  // token gid + 8
+      const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);  // head gid: tokens 2tig.., 8 + 2tig..
+      const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
+      // ---- O^T += V^T P^T: m-tile mt = dims 16mt .. 16mt + 15
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(swz_addr<D>(vb, (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a0, a1, a2, a3);
+        mma16<false>(o[mt], a0, a1, a2, a3, bh0, bh1);
+        mma16<false>(o[mt], a0, a1, a2, a3, bl0, bl1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[sg]);
+    }
+  }
+
+  // ================================================================ merge the consumer warps
+  __syncthreads();  // ring drained (every issued copy landed and was consumed)
+  float* mw = reinterpret_cast<float*>(smem);  // [NWC][G] max
+  float* lw = mw + NWC * G;                    // [NWC][G] sum
+  float* aw = lw + NWC * G;                    // [NWC][G][D] unnormalised output
+  if (warp < NWC) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float l = lrun[j];
+#pragma unroll
+      for (int m = 4; m <= 16; m <<= 1) l += shfl_xor(l, m);
+      const int g = 2 * tig + j;
+      if (g < G) {
+        if (gid == 0) {
+          mw[warp * G + g] = mrun[j];
+          lw[warp * G + g] = l;
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          aw[(warp * G + g) * D + 16 * mt + gid] = o[mt][j];
+          aw[(warp * G + g) * D + 16 * mt + gid + 8] = o[mt][2 + j];
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  const size_t out_row0 = static_cast<size_t>(b) * p.hq + hq0;
+  const bool single = (nsplit == 1 && npre == 0);
+  const bool with_prefix = CAS && (nsplit == 1 && npre > 0);
+  if (with_prefix) pdl_wait();
+  const size_t prec0 = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots;
+  for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
+    const int g = e / D, d = e % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NWC; ++w) M = fmaxf(M, mw[w * G + g]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWC; ++w) {
+      const float wt = fast_exp2(mw[w * G + g] - M);  // warps without blocks: 2^-inf = 0
+      num = fmaf(wt, aw[(w * G + g) * D + d], num);
+      den = fmaf(wt, lw[w * G + g], den);
+    }
+    if (CAS && with_prefix) {
+      float Mt = M;
+      for (int j = 0; j < npre; ++j) Mt = fmaxf(Mt, __ldcg(&p.part_ml[((prec0 + j) * G + g) * 2]));
+      float num2 = 0.f, den2 = 0.f;
+      if (Mt != -INFINITY) {
+        for (int j = 0; j < npre; ++j) {
+          const float wj = fast_exp2(__ldcg(&p.part_ml[((prec0 + j) * G + g) * 2]) - Mt);
+          num2 = fmaf(wj, __ldcg(&p.part_acc[((prec0 + j) * G + g) * D + d]), num2);
+          den2 = fmaf(wj, __ldcg(&p.part_ml[((prec0 + j) * G + g) * 2 + 1]), den2);
+        }
+        const float ws = fast_exp2(M - Mt);
+        num2 = fmaf(ws, num, num2);
+        den2 = fmaf(ws, den, den2);
+      }
+      const float ov = den2 > 0.f ? num2 / den2 : 0.f;
+      const size_t oi = (out_row0 + g) * D + d;
+      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = ov;
+      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov);
+    } else if (single) {
+      const float ov = num / den;
+      const size_t oi = (out_row0 + g) * D + d;
+      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = ov;
+      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov);
+    } else {
+      const size_t rec = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots + p.pre_slots + s;
+      p.part_acc[(rec * G + g) * D + d] = num;
+      if (d == 0) {
+        p.part_ml[(rec * G + g) * 2 + 0] = M;
+        p.part_ml[(rec * G + g) * 2 + 1] = den;
+      }
+    }
+  }
+  // A record was written (or, for one partition, the output): the merge kernel that
+  // follows combines the records.  A cascade grid completes only after the prefix pass,
+  // whose records the merge kernel also reads.
+  if constexpr (CAS) pdl_wait();
+}
+
+}  // namespace pkv

@@ -121,9 +121,10 @@ struct Split {
 };
 
 // Partitions of equal logical length (a multiple of 16 tokens), sized so that a batch at its
-// maximal length spreads over about four waves of CTAs (three resident per SM), clamped to
+// maximal length spreads over about three waves of CTAs (three resident per SM), clamped to
 // 512..2048 tokens: shorter partitions cost more merging and CTA start-up, longer ones leave
-// a long tail of lone CTAs.  PKV_SPLIT_TOKENS (a positive multiple of 16) overrides the
+// a long tail of lone CTAs (measured optimum of the tensor-core decode on the 8B-, 70B- and
+// shared-prefix-shaped steps).  PKV_SPLIT_TOKENS (a positive multiple of 16) overrides the
 // choice, for tuning and tests.
 Split choose_split(int batch, int hkv, int max_context_len, int sm_count) {
   const int max_nblk = (max_context_len + 15) / 16;
@@ -140,7 +141,7 @@ Split choose_split(int batch, int hkv, int max_context_len, int sm_count) {
   }
   if (sb == 0) {
     const long long units = static_cast<long long>(batch) * hkv;
-    const long long slots = 4LL * sm_count * 3;
+    const long long slots = 3LL * sm_count * 3;
     long long want = (static_cast<long long>(max_nblk) * units + slots - 1) / slots;
     if (want < kMinSplitBlocks) want = kMinSplitBlocks;
     if (want > kMaxSplitBlocks) want = kMaxSplitBlocks;
@@ -251,6 +252,7 @@ using InfoFn = pkv::DecodeLaunchInfo (*)();
 struct Variant {
   LaunchFn launch;
   InfoFn info;
+  bool swizzled = false;  // the tensor-core form reads 128-byte-swizzled 64-column boxes
 };
 
 template <int D, bool FP8, bool CAS>
@@ -264,8 +266,31 @@ Variant pick_g(int g) {
   }
 }
 
+template <int D, bool CAS>
+Variant pick_mma(int g) {
+  switch (g) {
+    case 1: return {pkv::launch_decode_mma<D, 1, CAS>, pkv::decode_mma_launch_info<D, 1, CAS>, true};
+    case 2: return {pkv::launch_decode_mma<D, 2, CAS>, pkv::decode_mma_launch_info<D, 2, CAS>, true};
+    case 4: return {pkv::launch_decode_mma<D, 4, CAS>, pkv::decode_mma_launch_info<D, 4, CAS>, true};
+    case 8: return {pkv::launch_decode_mma<D, 8, CAS>, pkv::decode_mma_launch_info<D, 8, CAS>, true};
+    default: return {nullptr, nullptr, false};
+  }
+}
+
+// bf16 pools take the tensor-core form unless PKV_DECODE_CUDA_CORES=1 asks for the
+// CUDA-core kernel (kept for E4M3 pools and for comparison).
+bool use_mma(bool fp8) {
+  if (fp8) return false;
+  const char* env = std::getenv("PKV_DECODE_CUDA_CORES");
+  return !(env && env[0] == '1');
+}
+
 // The plain decode, or the cascade variant that merges shared-prefix records.
 Variant pick_variant(int d, bool fp8, int g, bool cas) {
+  if (use_mma(fp8)) {
+    if (cas) return d == 64 ? pick_mma<64, true>(g) : pick_mma<128, true>(g);
+    return d == 64 ? pick_mma<64, false>(g) : pick_mma<128, false>(g);
+  }
   if (cas) {
     if (d == 64) return fp8 ? pick_g<64, true, true>(g) : pick_g<64, false, true>(g);
     return fp8 ? pick_g<128, true, true>(g) : pick_g<128, false, true>(g);
@@ -450,9 +475,14 @@ pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32
       return fail(PKV_ERR_WORKSPACE, "workspace has %zu bytes, %zu required", workspace_bytes, ws.total);
   }
   CUtensorMap tk, tv;
-  if (!encode_kv_map(&tk, cache->k_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8) ||
-      !encode_kv_map(&tv, cache->v_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8))
-    return fail(PKV_ERR_INVALID_ARG, "cannot describe the KV pool as a TMA tensor map");
+  const bool maps_ok =
+      var.swizzled ? encode_kv_map_sw128(&tk, cache->k_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim) &&
+                         encode_kv_map_sw128(&tv, cache->v_cache, cache->num_blocks, cache->num_kv_heads,
+                                             cache->head_dim)
+                   : encode_kv_map(&tk, cache->k_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8) &&
+                         encode_kv_map(&tv, cache->v_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim,
+                                       fp8);
+  if (!maps_ok) return fail(PKV_ERR_INVALID_ARG, "cannot describe the KV pool as a TMA tensor map");
 
   pkv::DecodeParams p{};
   p.q = static_cast<const uint16_t*>(q);
@@ -483,6 +513,12 @@ pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32
                   static_cast<unsigned>(sp.max_splits));
   cudaError_t e = var.launch(tk, tv, p, grid, reinterpret_cast<cudaStream_t>(stream), device);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (sp.max_splits > 1) {  // sequences split into several partitions: merge their records
+    e = pkv::launch_merge_partitions(cache->head_dim, num_q_heads / cache->num_kv_heads, fp8, p,
+                                     dim3(static_cast<unsigned>(cache->num_kv_heads), static_cast<unsigned>(batch)),
+                                     reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  }
   return PKV_OK;
 }
 
