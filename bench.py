@@ -89,6 +89,15 @@ def step_bytes(w: W.Workload) -> dict:
             "logical_kv": w.logical_kv_bytes()}
 
 
+def decode_kernel_name(cfg, cascade: bool) -> str:
+    """The kernels inside the decode call's timed interval (the merge runs only for split
+    sequences)."""
+    tc = cfg.kv_dtype == "bf16" and os.environ.get("PKV_DECODE_CUDA_CORES") != "1"
+    core = "paged_decode_mma_kernel (tensor cores)" if tc else "paged_decode_kernel (CUDA cores)"
+    name = core + " + merge_partitions_kernel"
+    return ("cascade_prefix_kernel + " + name) if cascade else name
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -100,7 +109,8 @@ def measured_peaks() -> dict:
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_17_gb300", "csrc")
-    for name in ("decode_kernel.cuh", "pkv_device.cuh", "decode_launch.cuh"):
+    for name in ("decode_kernel.cuh", "decode_mma.cuh", "mma_ops.cuh", "pkv_device.cuh", "decode_launch.cuh",
+                 "merge_partitions.cu"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -429,7 +439,7 @@ def run_ours(args):
         "decode_us": round(dec_avg_ms * 1e3, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None if cas is not None else ncu_traffic(cfg.name),
-                     "kernel": "cascade_prefix_kernel + paged_decode_kernel" if cas is not None else "paged_decode_kernel",
+                     "kernel": decode_kernel_name(cfg, cas is not None),
                      "peak_source": f"{peak_src} hbm_gbs (copy)",
                      "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
         "e2e": e2e,
