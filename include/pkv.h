@@ -138,19 +138,12 @@ pkv_status pkv_copy_blocks(const pkv_cache_desc* cache, const int64_t* block_pai
  * Bytes of device workspace that pkv_paged_decode_attention needs for these sizes on the
  * current device (0 if the call needs none, i.e. when no sequence is split).  The workspace
  * holds per-partition partial results (running max, running sum, unnormalised output) of
- * the context split, after a ticket region of fixed size (pkv_decode_workspace_tickets_bytes)
- * holding one int32 ticket per (sequence, kv head).
- * Contract: the ticket region must be zero before the first call that uses a workspace
- * (zero the whole buffer once when allocating it); every call that completes leaves it zero
- * again, whatever the sizes of the next call.  A workspace may not be used by two calls
- * that can run at the same time.
+ * the context split.  It needs no initialisation: every value a call reads was written by
+ * the same call.  A workspace may not be used by two calls that can run at the same time.
  * Returns 0 and sets pkv_last_error() for invalid sizes.
  */
 size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                  int32_t head_dim, int32_t max_context_len);
-
-/* Size of the ticket region at the start of every non-empty workspace (a constant). */
-size_t pkv_decode_workspace_tickets_bytes(void);
 
 /* Context partition length (tokens, a multiple of 16) the decode uses for these sizes on
  * the current device; a sequence of n tokens is split into ceil(n / partition) parts. */
@@ -174,8 +167,7 @@ int32_t pkv_decode_partition_tokens(int32_t batch, int32_t num_kv_heads, int32_t
  *   E4M3).  The result is deterministic: it depends only on the values, the lengths and
  *   the partition length, not on physical block ids, batch order or timing.
  *   workspace: device memory of at least pkv_decode_workspace_size(...) bytes, 256-byte
- *   aligned, with its ticket region zero on first use (see above); may be NULL when the
- *   required size is 0.
+ *   aligned, any contents; may be NULL when the required size is 0.
  */
 pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q,
                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -226,8 +218,7 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const
  *     count (its full table and length when it has no prefix); 0 is allowed when the
  *     prefix is the whole context.
  *   Other arguments as for pkv_paged_decode_attention; workspace of at least
- *   pkv_cascade_workspace_size(...) bytes (never 0 when prefixes exist), same zero-ticket
- *   contract.  E4M3 pools: the prefix pass expands the codes exactly to fp16 and multiplies
+ *   pkv_cascade_workspace_size(...) bytes (never 0 when prefixes exist), any contents.  E4M3 pools: the prefix pass expands the codes exactly to fp16 and multiplies
  *   in fp16 (q rounded to fp16, exact for |q| in 2^-14 .. 65504).  Both pools round the
  *   prefix softmax weights to the MMA's 16-bit type before the P V product.
  */

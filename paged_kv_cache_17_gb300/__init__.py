@@ -41,7 +41,7 @@ DEVFLAG_BAD_BLOCK_ID = 0x4
 DEVFLAG_WAIT_TIMEOUT = 0x8
 
 EXPORTED_SYMBOLS = (
-    "pkv_paged_kv_append", "pkv_decode_workspace_size", "pkv_decode_workspace_tickets_bytes",
+    "pkv_paged_kv_append", "pkv_decode_workspace_size",
     "pkv_decode_partition_tokens", "pkv_paged_decode_attention", "pkv_check_device_status",
     "pkv_status_string", "pkv_last_error", "pkv_version", "pkv_paged_decode_attention_noalloc",
     "pkv_copy_blocks", "pkv_cascade_workspace_size", "pkv_cascade_decode_attention",
@@ -77,8 +77,6 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_kv_append.argtypes = [ctypes.POINTER(CacheDesc), P, P, P, i64, P]
     lib.pkv_decode_workspace_size.restype = sz
     lib.pkv_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
-    lib.pkv_decode_workspace_tickets_bytes.restype = sz
-    lib.pkv_decode_workspace_tickets_bytes.argtypes = []
     lib.pkv_decode_partition_tokens.restype = i32
     lib.pkv_decode_partition_tokens.argtypes = [i32, i32, i32]
     lib.pkv_paged_decode_attention.restype = ctypes.c_int
@@ -187,12 +185,12 @@ def partition_tokens(batch: int, num_kv_heads: int, max_context_len: int) -> int
 
 
 def _workspace(device: torch.device, stream_handle: int, nbytes: int) -> torch.Tensor:
-    """A zero-initialised workspace per (device, stream), grown on demand.  The decode
-    kernels leave its ticket region zero, so it is reused without clearing."""
+    """A workspace per (device, stream), grown on demand (the decode needs nothing in it
+    initialised)."""
     key = (device.index if device.index is not None else torch.cuda.current_device(), stream_handle)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 

@@ -27,8 +27,8 @@
 //     rescale by exp(m_old - m_new) runs only when a running max actually moved;
 //   * the consumer warps' states are merged in shared memory; a single-partition sequence
 //     writes its output directly, otherwise the partition's (m, l, unnormalised acc) go to
-//     the workspace and the last CTA of (b, h) to finish -- found with an atomic ticket, no
-//     waiting -- merges the partitions in partition order with their log-sum-exp weights.
+//     the workspace and the merge kernel that follows (merge_partitions.cu) combines the
+//     partitions in partition order with their log-sum-exp weights.
 // Scores are kept in log2 units (q is pre-multiplied by scale*log2(e)), so every
 // exponential is one ex2.approx.
 #pragma once
@@ -43,7 +43,6 @@ struct DecodeParams {
   const int32_t* context_lens;  // [B]
   const float* scales;          // [2][Hkv] (E4M3) or nullptr
   void* out;                    // [B][Hq][D] bf16 or fp32
-  int32_t* tickets;             // [B][Hkv]        (multi-partition only)
   float* part_ml;               // [B][Hkv][rec_slots][G][2]
   float* part_acc;              // [B][Hkv][rec_slots][G][D]
   const int32_t* seq_prefix;    // [B]: >= 0 if the sequence has shared-prefix records, or nullptr
@@ -510,7 +509,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   float vfix = 1.0f;  // E4M3 values carry 2^-120; V's scale and that factor go to the output
   if constexpr (FP8) vfix = p.scales[p.hkv + h];
   const bool single = (nsplit == 1 && npre == 0);
-  // one partition and prefix records: merge them right here (no record, no ticket)
+  // one partition and prefix records: merge them right here (no record to write)
   const bool with_prefix = CAS && (nsplit == 1 && npre > 0);
   if (with_prefix) pdl_wait();
   const size_t prec0 = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots;

@@ -22,11 +22,6 @@ constexpr int kVersion = 100;  // 0.1.0
 constexpr int kMaxDevices = 64;
 constexpr int kMinSplitBlocks = 32;   // a context partition covers at least 512 tokens ...
 constexpr int kMaxSplitBlocks = 128;  // ... and at most 2048 (unless forced)
-// The workspace starts with a ticket region of fixed size, so a workspace reused for other
-// sizes never finds partial results of an earlier call where tickets are expected.  Launches
-// with more (sequence, kv head) units than tickets do not split the context: they already
-// have enough CTAs without it.
-constexpr long long kTickets = 65536;
 
 __device__ uint32_t g_pkv_status;  // PKV_DEVFLAG_* bits, one word per device
 
@@ -130,10 +125,6 @@ Split choose_split(int batch, int hkv, int max_context_len, int sm_count) {
   const int max_nblk = (max_context_len + 15) / 16;
   Split r{1, 1};
   if (max_nblk <= 0) return r;
-  if (static_cast<long long>(batch) * hkv > kTickets) {
-    r.split_blocks = max_nblk;
-    return r;
-  }
   int sb = 0;
   if (const char* env = std::getenv("PKV_SPLIT_TOKENS")) {
     const long v = std::strtol(env, nullptr, 10);
@@ -156,20 +147,19 @@ Split choose_split(int batch, int hkv, int max_context_len, int sm_count) {
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct WsLayout {
-  size_t tickets, ml, acc, total;
+  size_t ml, acc, total;
 };
 
 // Partial records per (sequence, kv head): pre_slots from a shared-prefix pass, then one per
 // context partition.  A plain decode with one partition needs no workspace.
 WsLayout ws_layout(int batch, int hkv, int g, int d, const Split& sp, int pre_slots) {
-  WsLayout w{0, 0, 0, 0};
+  WsLayout w{0, 0, 0};
   if (sp.max_splits <= 1 && pre_slots == 0) return w;
   const size_t units = static_cast<size_t>(batch) * hkv;
   const size_t slots = static_cast<size_t>(pre_slots) + sp.max_splits;
-  w.tickets = static_cast<size_t>(kTickets) * sizeof(int32_t);
   w.ml = round256(units * slots * g * 2 * sizeof(float));
   w.acc = round256(units * slots * g * d * sizeof(float));
-  w.total = w.tickets + w.ml + w.acc;
+  w.total = w.ml + w.acc;
   return w;
 }
 
@@ -374,7 +364,6 @@ int32_t pkv_decode_partition_tokens(int32_t batch, int32_t num_kv_heads, int32_t
   return choose_split(batch, num_kv_heads, max_context_len, dev->sm_count).split_blocks * 16;
 }
 
-size_t pkv_decode_workspace_tickets_bytes(void) { return static_cast<size_t>(kTickets) * sizeof(int32_t); }
 
 static pkv_status plan(int32_t batch, int32_t hq, int32_t hkv, int32_t d, int32_t max_len, bool fp8, Split* sp,
                        WsLayout* ws, Variant* var, DeviceInfo** devp, int pre_slots = 0) {
@@ -491,9 +480,8 @@ pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32
   p.scales = cache->scales;
   p.out = out;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  p.tickets = ws.total ? reinterpret_cast<int32_t*>(wsb) : nullptr;
-  p.part_ml = ws.total ? reinterpret_cast<float*>(wsb + ws.tickets) : nullptr;
-  p.part_acc = ws.total ? reinterpret_cast<float*>(wsb + ws.tickets + ws.ml) : nullptr;
+  p.part_ml = ws.total ? reinterpret_cast<float*>(wsb) : nullptr;
+  p.part_acc = ws.total ? reinterpret_cast<float*>(wsb + ws.ml) : nullptr;
   p.seq_prefix = pre_slots > 0 ? seq_prefix : nullptr;
   p.status = dev->status;
   p.max_blocks = max_blocks_per_seq;
@@ -603,8 +591,8 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   pr.indptr = px->member_indptr;
   pr.seqs = px->member_seqs;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  pr.part_ml = reinterpret_cast<float*>(wsb + ws.tickets);
-  pr.part_acc = reinterpret_cast<float*>(wsb + ws.tickets + ws.ml);
+  pr.part_ml = reinterpret_cast<float*>(wsb);
+  pr.part_acc = reinterpret_cast<float*>(wsb + ws.ml);
   pr.status = dev->status;
   pr.max_prefix_blocks = px->max_prefix_blocks;
   pr.max_members = px->max_members;

@@ -77,14 +77,8 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* c
     pkv_internal_set_error((std::string("cudaGetSymbolAddress(decode scratch): ") + cudaGetErrorString(e)).c_str());
     return PKV_ERR_CUDA;
   }
-  // The scratch keeps whatever the previous call left; the leading counters must start at
-  // zero, so clear them (completed calls leave them zero, an interrupted one might not).
-  const size_t head = pkv_decode_workspace_tickets_bytes();
-  if (need > 0) e = cudaMemsetAsync(ws, 0, need < head ? need : head, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    pkv_internal_set_error((std::string("clearing the decode scratch: ") + cudaGetErrorString(e)).c_str());
-    return PKV_ERR_CUDA;
-  }
+  // The scratch keeps whatever the previous call left; the decode needs nothing in it
+  // initialised (every record it reads was written by the same call).
   return pkv_paged_decode_attention(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
                                     max_context_len, softmax_scale, out, out_dtype, ws, kScratchBytes, stream);
 }
