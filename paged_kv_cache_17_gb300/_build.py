@@ -18,7 +18,8 @@ OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libpkv.so")
 SOURCES = ["pkv_api.cu", "append.cu", "decode_bf16.cu", "decode_e4m3.cu", "pkv_noalloc.cu", "copy_blocks.cu",
            "block_manager.cpp", "cascade_prefix.cu", "cascade_bf16.cu", "cascade_e4m3.cu",
-           "decode_mma.cu", "merge_partitions.cu"]
+           "decode_mma.cu", "decode_mma_e4m3.cu",
+           "merge_partitions.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

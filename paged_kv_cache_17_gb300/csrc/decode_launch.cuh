@@ -57,21 +57,29 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-// The tensor-core form (bf16 pools): same grid, ring depth and launch; 128-byte-swizzled
-// tensor maps.
-template <int D, int G, bool CAS>
+// The tensor-core form: same grid and launch; bf16 pools load 128-byte-swizzled boxes into
+// a 64 KiB ring, E4M3 pools raw boxes into a 32 KiB ring plus 8 KiB of expanded fp16 tiles
+// per consumer warp (three CTAs per SM either way).
+template <int D, bool FP8>
+struct MmaShape {
+  static constexpr int kNWC = 4;
+  static constexpr int kRingTile = FP8 ? 16 * D : 16 * D * 2;
+  static constexpr int kStages = (FP8 ? 32768 : 65536) / (2 * kRingTile);
+};
+
+template <int D, int G, bool FP8, bool CAS>
 DecodeLaunchInfo decode_mma_launch_info() {
-  using S = DecodeShape<D, false>;
-  using C = MmaCfg<D, G, S::kNWC, S::kStages>;
+  using S = MmaShape<D, FP8>;
+  using C = MmaCfg<D, G, FP8, S::kNWC, S::kStages>;
   return DecodeLaunchInfo{C::kThreads, C::kSmemBytes, C::kTilesBytes};
 }
 
-template <int D, int G, bool CAS>
+template <int D, int G, bool FP8, bool CAS>
 cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, dim3 grid,
                               cudaStream_t stream, int device) {
-  using S = DecodeShape<D, false>;
-  using C = MmaCfg<D, G, S::kNWC, S::kStages>;
-  auto kern = paged_decode_mma_kernel<D, G, S::kNWC, S::kStages, CAS>;
+  using S = MmaShape<D, FP8>;
+  using C = MmaCfg<D, G, FP8, S::kNWC, S::kStages>;
+  auto kern = paged_decode_mma_kernel<D, G, FP8, S::kNWC, S::kStages, CAS>;
   static bool configured[64] = {};
   if (device >= 0 && device < 64 && !configured[device]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
@@ -91,19 +99,21 @@ cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv, cons
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-#define PKV_DECLARE_DECODE_MMA(D, G, CAS)                                                                 \
-  extern template DecodeLaunchInfo decode_mma_launch_info<D, G, CAS>();                                   \
-  extern template cudaError_t launch_decode_mma<D, G, CAS>(const CUtensorMap&, const CUtensorMap&,       \
-                                                           const DecodeParams&, dim3, cudaStream_t, int);
-#define PKV_DEFINE_DECODE_MMA(D, G, CAS)                                                           \
-  template DecodeLaunchInfo decode_mma_launch_info<D, G, CAS>();                                   \
-  template cudaError_t launch_decode_mma<D, G, CAS>(const CUtensorMap&, const CUtensorMap&,       \
-                                                    const DecodeParams&, dim3, cudaStream_t, int);
-#define PKV_FOR_EACH_GROUP_MMA(M, D, CAS) M(D, 1, CAS) M(D, 2, CAS) M(D, 4, CAS) M(D, 8, CAS)
-PKV_FOR_EACH_GROUP_MMA(PKV_DECLARE_DECODE_MMA, 64, false)
-PKV_FOR_EACH_GROUP_MMA(PKV_DECLARE_DECODE_MMA, 128, false)
-PKV_FOR_EACH_GROUP_MMA(PKV_DECLARE_DECODE_MMA, 64, true)
-PKV_FOR_EACH_GROUP_MMA(PKV_DECLARE_DECODE_MMA, 128, true)
+#define PKV_DECLARE_DECODE_MMA(D, G, FP8, CAS)                                                              \
+  extern template DecodeLaunchInfo decode_mma_launch_info<D, G, FP8, CAS>();                                \
+  extern template cudaError_t launch_decode_mma<D, G, FP8, CAS>(const CUtensorMap&, const CUtensorMap&,    \
+                                                                const DecodeParams&, dim3, cudaStream_t, int);
+#define PKV_DEFINE_DECODE_MMA(D, G, FP8, CAS)                                                        \
+  template DecodeLaunchInfo decode_mma_launch_info<D, G, FP8, CAS>();                                \
+  template cudaError_t launch_decode_mma<D, G, FP8, CAS>(const CUtensorMap&, const CUtensorMap&,    \
+                                                         const DecodeParams&, dim3, cudaStream_t, int);
+#define PKV_FOR_EACH_GROUP_MMA(M, D, FP8, CAS) M(D, 1, FP8, CAS) M(D, 2, FP8, CAS) M(D, 4, FP8, CAS) M(D, 8, FP8, CAS)
+#define PKV_FOR_EACH_MMA(M)                                                                          \
+  PKV_FOR_EACH_GROUP_MMA(M, 64, false, false) PKV_FOR_EACH_GROUP_MMA(M, 128, false, false)          \
+  PKV_FOR_EACH_GROUP_MMA(M, 64, false, true) PKV_FOR_EACH_GROUP_MMA(M, 128, false, true)            \
+  PKV_FOR_EACH_GROUP_MMA(M, 64, true, false) PKV_FOR_EACH_GROUP_MMA(M, 128, true, false)            \
+  PKV_FOR_EACH_GROUP_MMA(M, 64, true, true) PKV_FOR_EACH_GROUP_MMA(M, 128, true, true)
+PKV_FOR_EACH_MMA(PKV_DECLARE_DECODE_MMA)
 
 // Explicit instantiations live in decode_bf16.cu / decode_e4m3.cu (plain) and
 // cascade_bf16.cu / cascade_e4m3.cu (cascade variants).

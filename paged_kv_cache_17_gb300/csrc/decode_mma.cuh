@@ -19,6 +19,11 @@
 // ldmatrix (V transposed); q stays in registers as B fragments; the weights P leave the S
 // accumulators through movmatrix (an 8x8 transpose inside the warp) as the B operand of
 // the second product, split into bf16 hi + lo so that P V keeps fp32-level accuracy.
+// E4M3 pools: the raw codes arrive in the ring; the consuming warp expands its tile exactly
+// to fp16 (cvt.rn.f16x2.e4m3x2) into a private swizzled tile, releases the ring slot, and
+// runs the products in fp16 -- q scaled per head by a power of two into fp16's range (the
+// factor is folded into that head's score scale), the K scale into the score scale, the V
+// scale into the output.
 #pragma once
 
 #include "decode_kernel.cuh"
@@ -26,35 +31,38 @@
 
 namespace pkv {
 
-template <int D, int G, int NWC, int STAGES>
+template <int D, int G, bool FP8, int NWC, int STAGES>
 struct MmaCfg {
   static constexpr int kHalves = D / 64;
-  static constexpr int kTileBytes = kBlockSize * D * 2;  // 16 rows x D bf16, as kHalves boxes
-  static constexpr int kKS = D / 16;                     // k-steps of the score product
-  static constexpr int kMT = D / 16;                     // m-tiles of the output product
+  static constexpr int kTileBytes = kBlockSize * D * 2;   // one 16-bit tile, as kHalves swizzled boxes
+  static constexpr int kRingTile = FP8 ? kBlockSize * D : kTileBytes;  // as loaded by TMA
+  static constexpr int kKS = D / 16;                      // k-steps of the score product
+  static constexpr int kMT = D / 16;                      // m-tiles of the output product
   static constexpr int kThreads = (NWC + 1) * 32;
-  static constexpr int kTilesBytes = 2 * STAGES * kTileBytes;
-  static constexpr int kBarOffset = kTilesBytes;
+  static constexpr int kRingBytes = 2 * STAGES * kRingTile;
+  static constexpr int kConvBytes = FP8 ? NWC * 2 * kTileBytes : 0;  // per warp: expanded K, V
+  static constexpr int kTilesBytes = kRingBytes;
+  static constexpr int kBarOffset = kRingBytes + kConvBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 2 * STAGES * 8;  // 1024: alignment slack
   static constexpr int kMergeBytes = NWC * (2 * G + G * D) * 4;
-  static_assert(kMergeBytes <= kTilesBytes, "merge scratch must fit in the tile ring");
+  static_assert(kMergeBytes <= kRingBytes, "merge scratch must fit in the tile ring");
   static_assert(G >= 1 && G <= 8, "a query group of at most 8 heads (the MMA's N)");
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(STAGES % NWC == 0, "each stage is always consumed by the same warp");
-  static_assert(kTileBytes % 1024 == 0, "1024-byte aligned boxes keep the swizzle aligned with the rows");
+  static_assert(kTileBytes % 1024 == 0 && kRingTile % 1024 == 0, "1024-byte aligned tiles");
 };
 
-template <int D, int G, int NWC, int STAGES, bool CAS>
+template <int D, int G, bool FP8, int NWC, int STAGES, bool CAS>
 __global__ void __launch_bounds__((NWC + 1) * 32)
     paged_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const DecodeParams p) {
-  using C = MmaCfg<D, G, NWC, STAGES>;
+  using C = MmaCfg<D, G, FP8, NWC, STAGES>;
   constexpr int KS = C::kKS, MT = C::kMT;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* k_tiles = smem;
-  uint8_t* v_tiles = smem + STAGES * C::kTileBytes;
+  uint8_t* v_tiles = smem + STAGES * C::kRingTile;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
   uint64_t* empty_bar = full_bar + STAGES;
 
@@ -84,7 +92,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
     if (s == 0) {
       if (CAS && npre > 0) {
         pdl_wait();
-        merge_records<D, G, false>(p, b, h, 0, npre, reinterpret_cast<float*>(smem), C::kThreads);
+        merge_records<D, G, FP8>(p, b, h, 0, npre, reinterpret_cast<float*>(smem), C::kThreads);
       } else {
         for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
           const size_t o = (static_cast<size_t>(b) * p.hq + hq0) * D + e;
@@ -108,6 +116,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   // q as the B operand of the score product: column n = head gid of the group (zero
   // columns past G), k = head_dim; one pair of bf16 words per k-step
   uint32_t qb[KS][2];
+  int qexp = 0;  // E4M3: q of head gid scaled by 2^qexp into fp16's range
   if (warp < NWC) {
     const bool live = gid < G;
     const uint32_t* qr = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(b) * p.hq + hq0 + (live ? gid : 0)) * D);
@@ -115,6 +124,23 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
     for (int kk = 0; kk < KS; ++kk) {
       qb[kk][0] = live ? qr[kk * 8 + tig] : 0u;      // dims 16kk + 2tig, +1
       qb[kk][1] = live ? qr[kk * 8 + 4 + tig] : 0u;  // dims 16kk + 8 + 2tig, +1
+    }
+    if constexpr (FP8) {
+      // the head's largest |q| (over the 4 lanes of equal gid) goes to 2^13 .. 2^14
+      float amax = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(qb[kk][e])), fabsf(bf16_hi(qb[kk][e]))));
+      amax = fmaxf(amax, shfl_xor(amax, 1));
+      amax = fmaxf(amax, shfl_xor(amax, 2));
+      qexp = amax > 0.f ? 13 - ilogbf(amax) : 0;
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          qb[kk][e] = pack_f16(ldexpf(bf16_lo(qb[kk][e]), qexp), ldexpf(bf16_hi(qb[kk][e]), qexp));
     }
   }
   if (threadIdx.x == NWC * 32) tma_prefetch_desc(&tm_k), tma_prefetch_desc(&tm_v);
@@ -127,7 +153,15 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   }
   __syncthreads();
 
-  const float sscale = p.score_scale;  // log2 units
+  // log2-domain score scale of this thread's two heads (2tig, 2tig+1); E4M3: times the K
+  // scale and 2^-qexp of that head
+  float sscale0 = p.score_scale, sscale1 = p.score_scale;
+  if constexpr (FP8) {
+    const int e0 = __shfl_sync(kFull, qexp, 4 * (2 * tig)), e1 = __shfl_sync(kFull, qexp, 4 * (2 * tig + 1));
+    const float ks = p.score_scale * p.scales[h];
+    sscale0 = ldexpf(ks, -e0);
+    sscale1 = ldexpf(ks, -e1);
+  }
   bool timed_out = false;
 
   if (warp == NWC) {
@@ -149,11 +183,16 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
           if (!timed_out) {
             // an id outside the pool reads a box entirely outside the tensor: zeros
             const int row0 = (pb >= 0 && pb < p.num_blocks) ? pb * kBlockSize : -kBlockSize;
-            mbar_arrive_expect_tx(&full_bar[st], 2 * C::kTileBytes);
+            mbar_arrive_expect_tx(&full_bar[st], 2 * C::kRingTile);
+            if constexpr (FP8) {  // one plain box of 16 rows x D codes per tile
+              tma_load_3d(k_tiles + st * C::kRingTile, &tm_k, 0, h, row0, &full_bar[st]);
+              tma_load_3d(v_tiles + st * C::kRingTile, &tm_v, 0, h, row0, &full_bar[st]);
+            } else {
 #pragma unroll
-            for (int hf = 0; hf < C::kHalves; ++hf) {
-              tma_load_3d(k_tiles + st * C::kTileBytes + hf * 2048, &tm_k, hf * 64, h, row0, &full_bar[st]);
-              tma_load_3d(v_tiles + st * C::kTileBytes + hf * 2048, &tm_v, hf * 64, h, row0, &full_bar[st]);
+              for (int hf = 0; hf < C::kHalves; ++hf) {
+                tma_load_3d(k_tiles + st * C::kRingTile + hf * 2048, &tm_k, hf * 64, h, row0, &full_bar[st]);
+                tma_load_3d(v_tiles + st * C::kRingTile + hf * 2048, &tm_v, hf * 64, h, row0, &full_bar[st]);
+              }
             }
           }
         }
@@ -190,9 +229,36 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         timed_out = true;
         break;
       }
-      const uint32_t kb = smem_u32(k_tiles + sg * C::kTileBytes);
-      const uint32_t vb = smem_u32(v_tiles + sg * C::kTileBytes);
+      uint32_t kb = smem_u32(k_tiles + sg * C::kRingTile);
+      uint32_t vb = smem_u32(v_tiles + sg * C::kRingTile);
       const int valid = min(kBlockSize, len - (blk0 + it) * kBlockSize);  // >= 1
+      if constexpr (FP8) {
+        // expand both tiles into this warp's fp16 tiles: 8 codes -> one swizzled 16-byte chunk
+        const uint32_t kc = smem_u32(smem + C::kRingBytes + warp * 2 * C::kTileBytes);
+        const uint32_t vc = kc + C::kTileBytes;
+        const uint8_t* rk = k_tiles + sg * C::kRingTile;
+        const uint8_t* rv = v_tiles + sg * C::kRingTile;
+        constexpr int kChunks = kBlockSize * (D / 8);
+#pragma unroll
+        for (int i = 0; i < 2 * kChunks / 32; ++i) {
+          const int ci = lane + 32 * i;
+          const bool isv = ci >= kChunks;
+          const int cj = isv ? ci - kChunks : ci;
+          const int r = cj / (D / 8), c = cj % (D / 8);
+          const uint2 raw = *reinterpret_cast<const uint2*>((isv ? rv : rk) + r * D + c * 8);
+          const uint32_t h0 = e4m3x2_to_f16x2(static_cast<uint16_t>(raw.x & 0xffffu));
+          const uint32_t h1 = e4m3x2_to_f16x2(static_cast<uint16_t>(raw.x >> 16));
+          const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(raw.y & 0xffffu));
+          const uint32_t h3 = e4m3x2_to_f16x2(static_cast<uint16_t>(raw.y >> 16));
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz_addr<D>(isv ? vc : kc, r, c)), "r"(h0),
+                       "r"(h1), "r"(h2), "r"(h3)
+                       : "memory");
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[sg]);  // the ring slot is free again
+        kb = kc;
+        vb = vc;
+      }
 
       // ---- S^T = K q^T: rows = tokens gid, gid+8; columns = heads 2tig, 2tig+1
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -200,12 +266,12 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       for (int kk = 0; kk < KS; ++kk) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(swz_addr<D>(kb, (lane & 7) + 8 * (mi & 1), 2 * kk + (mi >> 1)), a0, a1, a2, a3);
-        mma16<false>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        mma16<FP8>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int tok = gid + 8 * (e >> 1);
-        sc[e] = tok < valid ? sc[e] * sscale : -INFINITY;
+        sc[e] = tok < valid ? sc[e] * ((e & 1) ? sscale1 : sscale0) : -INFINITY;
       }
       // ---- online softmax per head: block max over the 16 tokens (lanes of equal tig)
       float bm0 = fmaxf(sc[0], sc[2]), bm1 = fmaxf(sc[1], sc[3]);
@@ -236,8 +302,8 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       lrun[1] += p1 + p3;
       // ---- P^T as the B operand: transpose (token, head-pair) fragments to (head, token-pair)
       uint32_t h01, l01, h23, l23;
-      split16<false>(p0, p1, h01, l01);  // token gid: heads 2tig, 2tig+1
-      split16<false>(p2, p3, h23, l23);  // token gid + 8
+      split16<FP8>(p0, p1, h01, l01);  // token gid: heads 2tig, 2tig+1
+      split16<FP8>(p2, p3, h23, l23);  // token gid + 8
       const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);  // head gid: tokens 2tig.., 8 + 2tig..
       const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
       // ---- O^T += V^T P^T: m-tile mt = dims 16mt .. 16mt + 15
@@ -245,11 +311,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       for (int mt = 0; mt < MT; ++mt) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4_t(swz_addr<D>(vb, (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a0, a1, a2, a3);
-        mma16<false>(o[mt], a0, a1, a2, a3, bh0, bh1);
-        mma16<false>(o[mt], a0, a1, a2, a3, bl0, bl1);
+        mma16<FP8>(o[mt], a0, a1, a2, a3, bh0, bh1);
+        mma16<FP8>(o[mt], a0, a1, a2, a3, bl0, bl1);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[sg]);
+      __syncwarp();  // the tiles are read (E4M3: this warp's fp16 tiles are rewritten next)
+      if (!FP8 && lane == 0) mbar_arrive(&empty_bar[sg]);
     }
   }
 
@@ -297,6 +363,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       num = fmaf(wt, aw[(w * G + g) * D + d], num);
       den = fmaf(wt, lw[w * G + g], den);
     }
+    if constexpr (FP8) num *= 7.52316384526264e-37f;  // 2^-120: the E4M3 record units
     if (CAS && with_prefix) {
       float Mt = M;
       for (int j = 0; j < npre; ++j) Mt = fmaxf(Mt, __ldcg(&p.part_ml[((prec0 + j) * G + g) * 2]));
@@ -311,12 +378,14 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         num2 = fmaf(ws, num, num2);
         den2 = fmaf(ws, den, den2);
       }
-      const float ov = den2 > 0.f ? num2 / den2 : 0.f;
+      float ov = den2 > 0.f ? num2 / den2 : 0.f;
+      if constexpr (FP8) ov = (ov * 1152921504606846976.0f) * (p.scales[p.hkv + h] * 1152921504606846976.0f);
       const size_t oi = (out_row0 + g) * D + d;
       if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = ov;
       else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov);
     } else if (single) {
-      const float ov = num / den;
+      float ov = num / den;
+      if constexpr (FP8) ov = (ov * 1152921504606846976.0f) * (p.scales[p.hkv + h] * 1152921504606846976.0f);
       const size_t oi = (out_row0 + g) * D + d;
       if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = ov;
       else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov);

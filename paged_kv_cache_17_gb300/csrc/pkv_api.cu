@@ -256,30 +256,33 @@ Variant pick_g(int g) {
   }
 }
 
-template <int D, bool CAS>
+template <int D, bool FP8, bool CAS>
 Variant pick_mma(int g) {
   switch (g) {
-    case 1: return {pkv::launch_decode_mma<D, 1, CAS>, pkv::decode_mma_launch_info<D, 1, CAS>, true};
-    case 2: return {pkv::launch_decode_mma<D, 2, CAS>, pkv::decode_mma_launch_info<D, 2, CAS>, true};
-    case 4: return {pkv::launch_decode_mma<D, 4, CAS>, pkv::decode_mma_launch_info<D, 4, CAS>, true};
-    case 8: return {pkv::launch_decode_mma<D, 8, CAS>, pkv::decode_mma_launch_info<D, 8, CAS>, true};
+    case 1: return {pkv::launch_decode_mma<D, 1, FP8, CAS>, pkv::decode_mma_launch_info<D, 1, FP8, CAS>, !FP8};
+    case 2: return {pkv::launch_decode_mma<D, 2, FP8, CAS>, pkv::decode_mma_launch_info<D, 2, FP8, CAS>, !FP8};
+    case 4: return {pkv::launch_decode_mma<D, 4, FP8, CAS>, pkv::decode_mma_launch_info<D, 4, FP8, CAS>, !FP8};
+    case 8: return {pkv::launch_decode_mma<D, 8, FP8, CAS>, pkv::decode_mma_launch_info<D, 8, FP8, CAS>, !FP8};
     default: return {nullptr, nullptr, false};
   }
 }
 
-// bf16 pools take the tensor-core form unless PKV_DECODE_CUDA_CORES=1 asks for the
-// CUDA-core kernel (kept for E4M3 pools and for comparison).
-bool use_mma(bool fp8) {
-  if (fp8) return false;
+// The tensor-core form unless PKV_DECODE_CUDA_CORES=1 asks for the CUDA-core kernel (kept
+// for comparison and tested).
+bool use_mma() {
   const char* env = std::getenv("PKV_DECODE_CUDA_CORES");
   return !(env && env[0] == '1');
 }
 
 // The plain decode, or the cascade variant that merges shared-prefix records.
 Variant pick_variant(int d, bool fp8, int g, bool cas) {
-  if (use_mma(fp8)) {
-    if (cas) return d == 64 ? pick_mma<64, true>(g) : pick_mma<128, true>(g);
-    return d == 64 ? pick_mma<64, false>(g) : pick_mma<128, false>(g);
+  if (use_mma()) {
+    if (fp8) {
+      if (cas) return d == 64 ? pick_mma<64, true, true>(g) : pick_mma<128, true, true>(g);
+      return d == 64 ? pick_mma<64, true, false>(g) : pick_mma<128, true, false>(g);
+    }
+    if (cas) return d == 64 ? pick_mma<64, false, true>(g) : pick_mma<128, false, true>(g);
+    return d == 64 ? pick_mma<64, false, false>(g) : pick_mma<128, false, false>(g);
   }
   if (cas) {
     if (d == 64) return fp8 ? pick_g<64, true, true>(g) : pick_g<64, false, true>(g);

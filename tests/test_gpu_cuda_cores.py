@@ -1,7 +1,7 @@
-"""The CUDA-core decode kernel (selected with PKV_DECODE_CUDA_CORES=1; bf16 pools otherwise
-take the tensor-core form, E4M3 pools always take this one) against the oracle, on the
-cases that cover its variants: full workloads, every head_dim / group size, partial blocks,
-forced partitions and the cascade merge."""
+"""The CUDA-core decode kernel (selected with PKV_DECODE_CUDA_CORES=1; by default every pool
+takes the tensor-core form) against the oracle, on the cases that cover its variants: full
+workloads, every head_dim / group size, partial blocks, forced partitions, E4M3 pools and
+the cascade merge."""
 import os
 
 import numpy as np
@@ -74,3 +74,16 @@ def test_cascade_merge(cuda_cores):
     ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
                             lens.numpy(), 0.1)
     assert_close(out.cpu().double().numpy(), ref, "bf16", "cuda cores cascade")
+
+
+@pytest.mark.parametrize("name", ["fp8_fork"])
+def test_e4m3_workload(cuda_cores, name):
+    w = W.make_workload(name)
+    _, out = gpu_step(w)
+    a, kc, vc = oracle_pools_after_append(w)
+    pairs = W.sample_pairs(w, 64, seed=6)
+    ref = oracle.decode_pairs(a["q"], kc, vc, oracle.KV_E4M3, a["block_tables"], a["context_lens"],
+                              w.cfg.softmax_scale, pairs, scales=a["scales"], nthreads=NT)
+    got = out.cpu().double().numpy()[pairs[:, 0], pairs[:, 1]]
+    assert_close(got, ref, "fp8", f"cuda cores {name}")
+    assert cuda_cores.check_device_status() == 0
