@@ -166,6 +166,12 @@ int32_t pkv_decode_partition_tokens(int32_t batch, int32_t num_kv_heads, int32_t
  *   K_t/V_t the cached rows of kv head hq/G at position t (decoded times its scale for
  *   E4M3).  The result is deterministic: it depends only on the values, the lengths and
  *   the partition length, not on physical block ids, batch order or timing.
+ *   Arithmetic: the per-block products run on the tensor cores with fp32 accumulation; K
+ *   and V enter as stored (bf16, or E4M3 expanded exactly to fp16); q enters as bf16, or
+ *   for E4M3 pools times a per-head power of two rounded to fp16 (relative error at most
+ *   2^-11); the softmax weights enter as a 16-bit hi + lo pair.  While the environment
+ *   variable PKV_DECODE_CUDA_CORES is "1" (read at each call), every product runs in fp32
+ *   on the CUDA cores instead.
  *   workspace: device memory of at least pkv_decode_workspace_size(...) bytes, 256-byte
  *   aligned, any contents; may be NULL when the required size is 0.
  */
