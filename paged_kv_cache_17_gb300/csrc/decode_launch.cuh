@@ -57,14 +57,17 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-// The tensor-core form: same grid and launch; bf16 pools load 128-byte-swizzled boxes into
-// a 64 KiB ring, E4M3 pools raw boxes into a 32 KiB ring plus 8 KiB of expanded fp16 tiles
-// per consumer warp (three CTAs per SM either way).
+// The tensor-core form: same grid and launch, a 32 KiB ring of K and V tiles.  bf16 pools:
+// 2 consumer warps and 128-byte-swizzled boxes (4 stages at D = 128; six CTAs per SM); E4M3
+// pools: 4 consumer warps, each expanding its own tiles into 8 KiB of fp16 (the expansion
+// is CUDA-core work that wants the extra warps; three CTAs per SM).  Measured against 4/8,
+// 2/6, 1/2 and 1/4 (warps/stages) on the 8B-shaped, 70B-shaped, short-suffix and fork
+// steps.
 template <int D, bool FP8>
 struct MmaShape {
-  static constexpr int kNWC = 4;
+  static constexpr int kNWC = FP8 ? 4 : 2;
   static constexpr int kRingTile = FP8 ? 16 * D : 16 * D * 2;
-  static constexpr int kStages = (FP8 ? 32768 : 65536) / (2 * kRingTile);
+  static constexpr int kStages = 32768 / (2 * kRingTile);
 };
 
 template <int D, int G, bool FP8, bool CAS>
