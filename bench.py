@@ -95,7 +95,7 @@ def decode_kernel_name(cfg, cascade: bool) -> str:
     tc = cfg.kv_dtype == "bf16" and os.environ.get("PKV_DECODE_CUDA_CORES") != "1"
     core = "paged_decode_mma_kernel (tensor cores)" if tc else "paged_decode_kernel (CUDA cores)"
     name = core + " + merge_partitions_kernel"
-    return ("cascade_prefix_kernel + " + name) if cascade else name
+    return ("cascade_prefix_tc_kernel (tcgen05) + " + name) if cascade else name
 
 
 def measured_peaks() -> dict:

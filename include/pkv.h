@@ -216,17 +216,20 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const
  * (prefix blocks of sequence b, if any) then (the blocks of block_tables row b), exactly
  * as pkv_paged_decode_attention over that concatenated table computes it, up to fp32
  * rounding.  The prefix part is computed once per prefix for all its member sequences,
- * as a dense [members x G rows] x [prefix keys] contraction on the tensor cores
- * (mma.sync, bf16 in, fp32 accumulate); the sequences' own blocks go through the decode
- * kernel, which merges the prefix results with log-sum-exp weights.
+ * as a dense [members x G rows] x [prefix keys] contraction on the fifth-generation tensor
+ * cores (tcgen05 MMAs of 128 query rows, fp32 accumulation in tensor memory); the
+ * sequences' own blocks go through the decode kernel, which merges the prefix results
+ * with log-sum-exp weights.
  *   prefixes: see pkv_prefix_desc; may describe zero prefixes (then this is a plain decode).
  *   block_tables / context_lens: each sequence's blocks AFTER its prefix and their token
  *     count (its full table and length when it has no prefix); 0 is allowed when the
  *     prefix is the whole context.
  *   Other arguments as for pkv_paged_decode_attention; workspace of at least
- *   pkv_cascade_workspace_size(...) bytes (never 0 when prefixes exist), any contents.  E4M3 pools: the prefix pass expands the codes exactly to fp16 and multiplies
- *   in fp16 (q rounded to fp16, exact for |q| in 2^-14 .. 65504).  Both pools round the
- *   prefix softmax weights to the MMA's 16-bit type before the P V product.
+ *   pkv_cascade_workspace_size(...) bytes (never 0 when prefixes exist), any contents.
+ *   Arithmetic of the prefix part: bf16 pools multiply bf16 q and K, and the softmax
+ *   weights enter the P V product as a bf16 hi + lo pair (about 16 significant bits);
+ *   E4M3 pools expand the codes exactly to fp16, multiply fp16 q (q rounded to fp16, exact
+ *   for |q| in 2^-14 .. 65504) and fp16 weights, whose rounded sum is the denominator.
  */
 typedef struct {
   const int32_t* prefix_tables;  /* [num_prefixes][max_prefix_blocks] physical block ids */

@@ -17,9 +17,9 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT_DIR, "libpkv.so")
 SOURCES = ["pkv_api.cu", "append.cu", "decode_bf16.cu", "decode_e4m3.cu", "pkv_noalloc.cu", "copy_blocks.cu",
-           "block_manager.cpp", "cascade_prefix.cu", "cascade_bf16.cu", "cascade_e4m3.cu",
+           "block_manager.cpp", "cascade_bf16.cu", "cascade_e4m3.cu",
            "decode_mma.cu", "decode_mma_e4m3.cu",
-           "merge_partitions.cu"]
+           "merge_partitions.cu", "cascade_prefix_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

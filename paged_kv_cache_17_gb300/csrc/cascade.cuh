@@ -31,17 +31,20 @@ struct PrefixParams {
   const float* scales;  // [2][Hkv] (E4M3 pools) or nullptr
 };
 
-// bf16 pools take the 128-byte-swizzled 64-column tensor maps, E4M3 pools the plain ones
+
+// The prefix pass on the tcgen05 tensor cores (cascade_prefix_tc.cu): 128-row query tiles;
+// bf16 pools are read through the 128-byte-swizzled 64-column tensor maps, E4M3 pools
+// through the plain ones.
 template <int D, bool FP8>
-cudaError_t launch_cascade_prefix(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p, dim3 grid,
-                                  cudaStream_t stream, int device);
-#define PKV_DECLARE_PREFIX(D, FP8)                                                                              \
-  extern template cudaError_t launch_cascade_prefix<D, FP8>(const CUtensorMap&, const CUtensorMap&,            \
-                                                            const PrefixParams&, dim3, cudaStream_t, int);
-PKV_DECLARE_PREFIX(64, false)
-PKV_DECLARE_PREFIX(128, false)
-PKV_DECLARE_PREFIX(64, true)
-PKV_DECLARE_PREFIX(128, true)
-#undef PKV_DECLARE_PREFIX
+cudaError_t launch_cascade_prefix_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p, dim3 grid,
+                                     cudaStream_t stream, int device);
+#define PKV_DECLARE_PREFIX_TC(D, FP8)                                                                        \
+  extern template cudaError_t launch_cascade_prefix_tc<D, FP8>(const CUtensorMap&, const CUtensorMap&,      \
+                                                               const PrefixParams&, dim3, cudaStream_t, int);
+PKV_DECLARE_PREFIX_TC(64, false)
+PKV_DECLARE_PREFIX_TC(128, false)
+PKV_DECLARE_PREFIX_TC(64, true)
+PKV_DECLARE_PREFIX_TC(128, true)
+#undef PKV_DECLARE_PREFIX_TC
 
 }  // namespace pkv

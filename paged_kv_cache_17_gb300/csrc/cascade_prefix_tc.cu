@@ -1,0 +1,597 @@
+// cascade_prefix_tc.cu -- the shared-prefix pass of cascade decode on the fifth-generation
+// tensor cores (tcgen05 MMAs accumulating in tensor memory).
+//
+// habr.com/ru/articles/1021832, section 7 "Тот самый Cache Read", and
+// ml-canon.vercel.app/54-prefix-caching-cacheblend.html, "Идея и механизм": requests that
+// start with the same prompt share that prompt's KV blocks, identical for every one of
+// them.  Section 3 of the habr article ("Вспомним FlashAttention") gives the exact split:
+// attention over one part of the keys is a running max m, a running sum l and an
+// unnormalised output, and parts combine with the rescale exp(m_part - m_total).  So the
+// prefix part of every member's decode attention is computed here once per prefix group;
+// each sequence's own blocks are handled by the decode kernel, which merges these partial
+// results as extra partitions.  Per (kv head, prefix) the contraction is [member rows x
+// prefix keys], dense and large enough for the 128-row MMAs:
+//
+//   S [128 rows x 64 keys] = Q [128 x D] K^T          (tcgen05.mma kind::f16, fp32 in TMEM)
+//   P = 2^(S * scale - m)                             (one thread per row, CUDA cores)
+//   O [128 x D]          += P [128 x 64] V [64 x D]   (O stays in TMEM for the whole split)
+//
+// CTA = 128 query rows (row r: member r / G, query head h * G + r % G), one kv head, one
+// split of the prefix (a run of whole 64-key stages):
+//   warps 0-3  softmax: thread r owns row r (TMEM lane r); reads S, writes P as 16-bit
+//              values into the stage's K tile (K is no longer needed once S is computed),
+//              rescales its O row when its reference max moved, and writes the record;
+//              bf16 pools write P as bf16 hi + lo (lo = P - hi rounded, in a buffer of its
+//              own), and O += P V runs once for each, so the weights keep about 16 bits;
+//   warp 4     lane 0 issues every MMA;
+//   warp 5     the producer: block ids of the split 32 at a time in its lanes, one TMA box
+//              per (block, 64 columns, K or V) into the ring as slots come free;
+//   warps 6-9  (E4M3 pools) expand each raw stage exactly to fp16 into a 16-bit ring.
+// S is double-buffered in TMEM, so the tensor cores compute S of stage t + 2 and O of stage
+// t while the softmax warps work on stage t + 1.  The reference max of a row changes only
+// when the row max exceeds it by more than 2^8 (weights then stay <= 256, exact in bf16 and
+// fp16 range), so O is rescaled rarely; the record carries the reference max it used.
+//
+// Shared memory: Q (128 x D, 16-bit, 128-byte swizzled, K-major), a 4-stage TMA ring of K
+// and V tiles ([column half][64 keys][128 bytes], swizzled by the TMA load), for E4M3 a
+// 3-stage ring of expanded fp16 tiles; D = 64 gives P two buffers of its own, bf16 pools
+// two more for the lo parts.  TMEM: S at
+// columns 0 and 64, O at column 128 (256 columns; one or two CTAs per SM).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "cascade.cuh"
+#include "mma_ops.cuh"
+#include "pkv_device.cuh"
+#include "tc_ops.cuh"
+
+namespace pkv {
+
+template <int D, bool FP8>
+struct TcPrefixCfg {
+  static constexpr int kRows = 128;             // query rows per CTA: the MMA's M
+  static constexpr int kKeys = 64;              // keys per stage: N of S, K of O += P V
+  static constexpr int kStageBlocks = kKeys / kBlockSize;
+  static constexpr int kRing = 4;               // TMA ring depth
+  static constexpr int kExp = 3;                // E4M3: expanded 16-bit stages
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQHalf = kRows * 128;    // one 64-column half of Q
+  static constexpr int kHalf16 = kKeys * 128;   // one 64-column half of a 16-bit K or V stage
+  static constexpr int kTile16 = kHalves * kHalf16;
+  static constexpr int kRaw = FP8 ? kKeys * D : kTile16;  // a K or V stage as loaded
+  static constexpr int kPBytes = kRows * kKeys * 2;
+  static constexpr bool kPInK = kTile16 >= kPBytes;
+  static constexpr bool kPSplit = !FP8;         // bf16 weights as hi + lo (two P V products)
+  static constexpr int kPBufs = (kPInK ? 0 : 2) + (kPSplit ? 2 : 0);
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffRawK = kOffQ + kHalves * kQHalf;
+  static constexpr int kOffRawV = kOffRawK + kRing * kRaw;
+  static constexpr int kOffExpK = kOffRawV + kRing * kRaw;
+  static constexpr int kOffExpV = kOffExpK + (FP8 ? kExp * kTile16 : 0);
+  static constexpr int kOffP = kOffExpV + (FP8 ? kExp * kTile16 : 0);
+  static constexpr int kOffBar = kOffP + kPBufs * kPBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kBytes = 1024 + kOffBar + kBarBytes;  // 1024: alignment slack
+  static constexpr int kColS = 0, kColO = 128, kTmemCols = 256;
+  static constexpr int kSoftWarps = 4, kIssuerWarp = 4, kProducerWarp = 5, kConvWarp0 = 6;
+  static constexpr int kConvWarps = FP8 ? 4 : 0;
+  static constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;
+  static constexpr float kLazy = 8.f;           // log2 of the largest weight before a rescale
+  static_assert(D == 64 || D == 128, "head_dim");
+  static_assert(kRaw % 1024 == 0 && kTile16 % 1024 == 0 && kPBytes % 1024 == 0, "1024-byte aligned tiles");
+  static_assert(kColO + D <= kTmemCols, "TMEM columns");
+};
+
+namespace {
+
+// wait for a phase, giving up when the CTA has aborted or after the wait limit
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long start = clock64();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - start > kWaitLimitCycles) return false;
+  }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+}  // namespace
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
+    cascade_prefix_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                             const PrefixParams p) {
+  using C = TcPrefixCfg<D, FP8>;
+  constexpr int R = C::kRing, E = C::kExp;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);  // [R] TMA landed
+  uint64_t* empty = full + R;        // [R] bf16: O += P V of the slot's stage done
+  uint64_t* raw_empty = empty + R;   // [R] E4M3: the slot's raw stage expanded
+  uint64_t* exp_full = raw_empty + R;  // [E] E4M3: stage expanded
+  uint64_t* exp_empty = exp_full + E;  // [E] E4M3: O += P V of the slot's stage done
+  uint64_t* s_full = exp_empty + E;  // [2] S of a stage done
+  uint64_t* p_full = s_full + 2;     // [2] P of a stage written (one arrival per softmax warp)
+  uint64_t* o_done = p_full + 2;     // O += P V of a stage done
+  uint64_t* drain = o_done + 1;      // every MMA issued so far done (abort path)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tile = blockIdx.x;
+  const int h = blockIdx.y;
+  const int pfx = blockIdx.z / p.pre_slots;
+  const int split = blockIdx.z % p.pre_slots;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  pdl_wait();
+  // the decode kernel that follows may start now: what it reads before waiting for this
+  // grid (the pool after the append) is complete once every CTA is past the wait above
+  pdl_launch_dependents();
+
+  const int m0 = p.indptr[pfx], m1 = p.indptr[pfx + 1];
+  int members = m1 - m0;
+  if (members < 0 || members > p.max_members) {  // the grid covers max_members members
+    if (threadIdx.x == 0 && tile == 0 && split == 0 && h == 0) set_flag(p.status, PKV_DEVFLAG_BAD_CONTEXT_LEN);
+    members = max(0, min(members, p.max_members));
+  }
+  const int G = p.group;
+  const int rows = members * G;
+  if (tile * C::kRows >= rows) return;
+  int plen = p.prefix_lens[pfx];
+  if (plen < 0 || plen > p.max_prefix_blocks * kBlockSize || (plen & (kBlockSize - 1))) {
+    if (threadIdx.x == 0 && tile == 0 && split == 0 && h == 0) set_flag(p.status, PKV_DEVFLAG_BAD_CONTEXT_LEN);
+    plen = max(0, min(plen, p.max_prefix_blocks * kBlockSize)) & ~(kBlockSize - 1);
+  }
+  const int pblocks = plen / kBlockSize;
+  const int blk0 = min(pblocks, split * p.split_blocks);
+  const int blk1 = min(pblocks, blk0 + p.split_blocks);
+  const int nstage = (blk1 - blk0 + C::kStageBlocks - 1) / C::kStageBlocks;
+  const int32_t* table = p.prefix_tables + static_cast<size_t>(pfx) * p.max_prefix_blocks;
+
+  // ---- the row of a softmax thread
+  const bool soft = warp < C::kSoftWarps;
+  const int r = threadIdx.x;  // softmax threads: row r of the tile, TMEM lane r
+  bool rv = false;
+  int rb = 0, rg = 0;
+  if (soft) {
+    const int row = tile * C::kRows + r;
+    rv = row < rows;
+    if (rv) {
+      rg = row % G;
+      rb = p.seqs[m0 + row / G];
+      if (rb < 0 || rb >= p.batch) {
+        set_flag(p.status, PKV_DEVFLAG_BAD_BLOCK_ID);
+        rv = false;
+        rb = 0;
+      }
+    }
+  }
+  const float vunit = FP8 ? 7.52316384526264e-37f : 1.0f;  // 2^-120: the decode kernel's E4M3 units
+  auto write_record = [&](float m, float l, int chunk, const float* o32) {
+    // chunk < 0: m and l; else 32 output columns starting at 32 * chunk
+    const size_t rec = (static_cast<size_t>(rb) * p.hkv + h) * p.rec_slots + split;
+    const size_t base = rec * G + rg;
+    if (chunk < 0) {
+      p.part_ml[base * 2 + 0] = m;
+      p.part_ml[base * 2 + 1] = l;
+    } else {
+      float4* dst = reinterpret_cast<float4*>(p.part_acc + base * D + 32 * chunk);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(o32[4 * i] * vunit, o32[4 * i + 1] * vunit, o32[4 * i + 2] * vunit,
+                             o32[4 * i + 3] * vunit);
+    }
+  };
+  if (nstage == 0) {  // an empty split: m = -inf, l = 0, o = 0
+    if (soft && rv) {
+      float z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0.f;
+      write_record(-INFINITY, 0.f, -1, z);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) write_record(0.f, 0.f, c, z);
+    }
+    return;
+  }
+
+  // ---- Q rows -> shared memory, K-major 128-byte swizzle (16-bit; fp16 for E4M3 pools)
+  const uint32_t q_base = smem_u32(smem + C::kOffQ);
+  if (soft) {
+    const uint4* qr = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(rb) * p.hq + h * G + rg) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      uint4 v = rv ? qr[c] : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (FP8) {
+        v.x = pack_f16(bf16_lo(v.x), bf16_hi(v.x));
+        v.y = pack_f16(bf16_lo(v.y), bf16_hi(v.y));
+        v.z = pack_f16(bf16_lo(v.z), bf16_hi(v.z));
+        v.w = pack_f16(bf16_lo(v.w), bf16_hi(v.w));
+      }
+      st_shared_v4(q_base + (c >> 3) * C::kQHalf + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4), v.x,
+                   v.y, v.z, v.w);
+    }
+    fence_proxy_async_smem();  // read by the tensor cores
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == C::kIssuerWarp * 32) {
+    for (int i = 0; i < R; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+      mbar_init(&raw_empty[i], 1);
+    }
+    for (int i = 0; i < E; ++i) {
+      mbar_init(&exp_full[i], 1);
+      mbar_init(&exp_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], C::kSoftWarps);  // one arrival per softmax warp
+    }
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
+    *abort = 1;
+  };
+  // TMA of stage t into ring slot t % R: block j of the stage starts at pool row row0[j]
+  // (-16 for blocks past the split: a box entirely outside the tensor reads zeros)
+  auto tma_stage = [&](int t, const int (&row0)[C::kStageBlocks]) {
+    const int st = t % R;
+    mbar_arrive_expect_tx(&full[st], 2 * C::kRaw);
+#pragma unroll
+    for (int j = 0; j < C::kStageBlocks; ++j) {
+      if constexpr (FP8) {
+        const int off = st * C::kRaw + j * kBlockSize * D;
+        tma_load_3d(smem + C::kOffRawK + off, &tm_k, 0, h, row0[j], &full[st]);
+        tma_load_3d(smem + C::kOffRawV + off, &tm_v, 0, h, row0[j], &full[st]);
+      } else {
+#pragma unroll
+        for (int hf = 0; hf < C::kHalves; ++hf) {
+          const int off = st * C::kRaw + hf * C::kHalf16 + j * 2048;
+          tma_load_3d(smem + C::kOffRawK + off, &tm_k, hf * 64, h, row0[j], &full[st]);
+          tma_load_3d(smem + C::kOffRawV + off, &tm_v, hf * 64, h, row0[j], &full[st]);
+        }
+      }
+    }
+  };
+  // the 16-bit K and V tiles and the P buffer of stage t
+  auto k_tile = [&](int t) -> uint32_t {
+    return FP8 ? smem_u32(smem + C::kOffExpK + (t % E) * C::kTile16) : smem_u32(smem + C::kOffRawK + (t % R) * C::kRaw);
+  };
+  auto v_tile = [&](int t) -> uint32_t {
+    return FP8 ? smem_u32(smem + C::kOffExpV + (t % E) * C::kTile16) : smem_u32(smem + C::kOffRawV + (t % R) * C::kRaw);
+  };
+  // P (or its hi part) of stage t: the stage's K tile, else one of two buffers; the lo part
+  // of bf16 weights: two buffers after those (a buffer is rewritten two stages later, when
+  // S of that stage is done, which implies O += P V of this stage is done)
+  auto p_tile = [&](int t) -> uint32_t {
+    return C::kPInK ? k_tile(t) : smem_u32(smem + C::kOffP + (t & 1) * C::kPBytes);
+  };
+  auto plo_tile = [&](int t) -> uint32_t {
+    return smem_u32(smem + C::kOffP + ((C::kPInK ? 0 : 2) + (t & 1)) * C::kPBytes);
+  };
+
+  if (warp == C::kIssuerWarp) {
+    // ======================================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_f16(C::kRows, C::kKeys, !FP8, false);
+      constexpr uint32_t kIdO = idesc_f16(C::kRows, D, !FP8, true);
+      // S(t) into buffer t % 2: D/16 k-steps of 16 head dims (byte 32k of a 128-byte row)
+      auto issue_s = [&](int t) {
+        const uint32_t kt = k_tile(t);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = sdesc_sw128(q_base + (kk >> 2) * C::kQHalf + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(kt + (kk >> 2) * C::kHalf16 + (kk & 3) * 32, 16, 1024);
+          mma_f16_ss(tmem + C::kColS + 64 * (t & 1), a, b, kIdS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[t & 1]);
+      };
+      // O += P(t) V(t): 4 k-steps of 16 keys; V is MN-major (64 head dims per 128-byte row)
+      auto issue_o = [&](int t) {
+        const uint32_t pt = p_tile(t), vt = v_tile(t);
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < C::kKeys / 16; ++j) {
+          const uint64_t a = sdesc_sw128(pt + j * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(vt + j * 2048, C::kHalf16, 1024);
+          mma_f16_ss(tmem + C::kColO, a, b, kIdO, (t > 0 || j > 0) ? 1u : 0u);
+          if constexpr (C::kPSplit) mma_f16_ss(tmem + C::kColO, sdesc_sw128(plo_tile(t) + j * 32, 16, 1024), b, kIdO, 1u);
+        }
+        tc_commit(FP8 ? &exp_empty[t % E] : &empty[t % R]);
+        tc_commit(o_done);
+      };
+      auto wait_tiles = [&](int t) -> bool {
+        if constexpr (FP8) return wait_or_abort(&exp_full[t % E], (t / E) & 1, abort);
+        return wait_or_abort(&full[t % R], (t / R) & 1, abort);
+      };
+      bool ok = true;
+      for (int t = 0; t < min(2, nstage) && ok; ++t) {
+        ok = wait_tiles(t);
+        if (ok) issue_s(t);
+      }
+      for (int t = 0; t < nstage && ok; ++t) {
+        ok = wait_or_abort(&p_full[t & 1], (t >> 1) & 1, abort);
+        if (!ok) break;
+        issue_o(t);
+        if (t + 2 < nstage) {
+          ok = wait_tiles(t + 2);
+          if (!ok) break;
+          issue_s(t + 2);
+        }
+      }
+      if (!ok && !*abort) fail();
+      // nothing may run on the tensor cores when the CTA frees its tensor memory
+      tc_commit(drain);
+      mbar_wait(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp == C::kProducerWarp) {
+    // ======================================================================== TMA producer
+    // block ids of the split, 32 (eight stages) at a time in the lanes, the next 32 in flight
+    const int nblk = blk1 - blk0;
+    int ids = lane < nblk ? table[blk0 + lane] : 0;
+    int nxt = 32 + lane < nblk ? table[blk0 + 32 + lane] : 0;
+    int issued = 0;
+    bool ok = true;
+    for (int t = 0; t < nstage; ++t) {
+      const int st = t % R;
+      if (t >= R) {  // the slot's previous stage is consumed
+        ok = wait_or_abort(FP8 ? &raw_empty[st] : &empty[st], ((t / R) - 1) & 1, abort);
+        if (!__all_sync(kFull, ok)) {
+          ok = false;
+          break;
+        }
+      }
+      const int w0 = (t * C::kStageBlocks) & 31;
+      if (t > 0 && w0 == 0) {
+        ids = nxt;
+        const int k = t * C::kStageBlocks + 32 + lane;
+        nxt = k < nblk ? table[blk0 + k] : 0;
+      }
+      int row0[C::kStageBlocks];
+#pragma unroll
+      for (int j = 0; j < C::kStageBlocks; ++j) {
+        const int pb = __shfl_sync(kFull, ids, w0 + j);
+        row0[j] = -kBlockSize;
+        if (t * C::kStageBlocks + j < nblk) {
+          if (pb >= 0 && pb < p.num_blocks) row0[j] = pb * kBlockSize;
+          else if (lane == 0) set_flag(p.status, PKV_DEVFLAG_BAD_BLOCK_ID);
+        }
+      }
+      if (lane == 0) tma_stage(t, row0);
+      issued = t + 1;
+    }
+    if (lane == 0) {
+      if (!ok && !*abort) fail();
+      // nothing may be in flight when the CTA exits: the last stages issued have landed
+      for (int t = max(0, issued - R); t < issued; ++t)
+        if (!mbar_wait(&full[t % R], (t / R) & 1)) break;
+    }
+    __syncwarp();
+  } else if (!soft) {
+    // ======================================================================== E4M3 expansion
+    if constexpr (FP8) {
+      const int ct = threadIdx.x - C::kConvWarp0 * 32;  // 0 .. 127
+      constexpr int kChunks = C::kKeys * (D / 8);  // 8-code chunks per tile
+      for (int t = 0; t < nstage; ++t) {
+        const int rs = t % R, es = t % E;
+        bool ok = wait_or_abort(&full[rs], (t / R) & 1, abort);
+        if (ok && t >= E) ok = wait_or_abort(&exp_empty[es], ((t / E) - 1) & 1, abort);
+        if (!ok && !*abort) fail();
+        if (ok) {
+          const uint8_t* rk = smem + C::kOffRawK + rs * C::kRaw;
+          const uint8_t* rvv = smem + C::kOffRawV + rs * C::kRaw;
+          const uint32_t ek = smem_u32(smem + C::kOffExpK + es * C::kTile16);
+          const uint32_t ev = smem_u32(smem + C::kOffExpV + es * C::kTile16);
+#pragma unroll 4
+          for (int i = 0; i < 2 * kChunks / 128; ++i) {
+            const int ci = ct + 128 * i;
+            const bool isv = ci >= kChunks;
+            const int cj = isv ? ci - kChunks : ci;
+            const int kr = cj / (D / 8), c = cj % (D / 8);
+            const uint2 raw = *reinterpret_cast<const uint2*>((isv ? rvv : rk) + kr * D + c * 8);
+            const uint32_t dst =
+                (isv ? ev : ek) + (c >> 3) * C::kHalf16 + (kr >> 3) * 1024 + (kr & 7) * 128 + (((c & 7) ^ (kr & 7)) << 4);
+            st_shared_v4(dst, e4m3x2_to_f16x2(static_cast<uint16_t>(raw.x & 0xffffu)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(raw.x >> 16)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(raw.y & 0xffffu)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(raw.y >> 16)));
+          }
+        }
+        fence_proxy_async_smem();  // the expanded tiles are read by the tensor cores
+        // every converter thread reaches this, failed or not, and all leave together
+        if (named_sync_or(1, 128, *abort != 0)) break;
+        if (ct == 0) {
+          mbar_arrive(&raw_empty[rs]);  // the raw slot is read
+          mbar_arrive(&exp_full[es]);   // the expanded stage is complete
+        }
+      }
+    }
+  } else {
+    // ======================================================================== softmax
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sscale = FP8 ? p.score_scale * p.scales[h] : p.score_scale;
+    float m_used = -INFINITY, l = 0.f;
+    for (int t = 0; t < nstage; ++t) {
+      const int b = t & 1;
+      bool ok = wait_or_abort(&s_full[b], (t >> 1) & 1, abort);
+      if (!__all_sync(kFull, ok)) {  // tcgen05.ld is warp-collective: leave as a warp
+        if (!*abort) fail();
+        break;
+      }
+      tc_fence_after();
+      float sv[64];
+      tmem_ld64(tmem + lane_base + C::kColS + 64 * b, sv);
+      const int nkeys = min(C::kKeys, (blk1 - blk0 - t * C::kStageBlocks) * kBlockSize);
+      // keys past the split (the last stage only) take no part in the extreme below and get
+      // weight 0; the row max of the scaled scores is the scale times the max (scale >= 0)
+      // or the min (scale < 0) of the raw scores
+      const bool partial = nkeys < C::kKeys;
+      if (partial) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i >= nkeys) sv[i] = sscale >= 0.f ? -INFINITY : INFINITY;
+      }
+      float ext = sv[0];
+      if (sscale >= 0.f) {
+#pragma unroll
+        for (int i = 1; i < 64; ++i) ext = fmaxf(ext, sv[i]);
+      } else {
+#pragma unroll
+        for (int i = 1; i < 64; ++i) ext = fminf(ext, sv[i]);
+      }
+      const float mx = ext * sscale;
+      const bool grow = mx > m_used + C::kLazy;  // always at t = 0 (every stage has a key)
+      float alpha = 1.f;
+      if (grow) {
+        alpha = fast_exp2(m_used - mx);  // 0 at t = 0
+        l *= alpha;
+        m_used = mx;
+      }
+      const float negm = -m_used;
+      // P row r: 64 weights 2^(s * scale - m) <= 2^8 as 16-bit values, 128-byte swizzled
+      // K-major (8 chunks of 8 keys).  bf16 pools: hi + lo parts (about 16 bits together)
+      // and l sums the fp32 weights; E4M3 pools: fp16 weights and l sums the rounded ones,
+      // so O / l weighs V by the weights the MMAs use
+      const uint32_t roff = (r >> 3) * 1024 + (r & 7) * 128;
+      const uint32_t prow = p_tile(t) + roff;
+      const uint32_t plrow = C::kPSplit ? plo_tile(t) + roff : 0u;
+      float ls = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4], wl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k = 8 * c + 2 * e;
+          float a = fast_exp2(fmaf(sv[k], sscale, negm));
+          float bb = fast_exp2(fmaf(sv[k + 1], sscale, negm));
+          if (partial) {  // a zero scale makes the masked products NaN: weight 0 by selection
+            a = k < nkeys ? a : 0.f;
+            bb = k + 1 < nkeys ? bb : 0.f;
+          }
+          if constexpr (C::kPSplit) {
+            w[e] = pack_bf16(a, bb);
+            wl[e] = pack_bf16(a - __uint_as_float(w[e] << 16), bb - __uint_as_float(w[e] & 0xffff0000u));
+            ls += a + bb;
+          } else {
+            w[e] = pack_f16(a, bb);
+            ls += sum16<true>(w[e]);
+          }
+        }
+        st_shared_v4(prow + ((c ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+        if constexpr (C::kPSplit) st_shared_v4(plrow + ((c ^ (r & 7)) << 4), wl[0], wl[1], wl[2], wl[3]);
+      }
+      l += ls;
+      // rescale O where this warp's rows moved their reference max (after O += P V of t - 1)
+      if (t > 0 && __any_sync(kFull, grow)) {
+        ok = wait_or_abort(o_done, (t - 1) & 1, abort);
+        if (!__all_sync(kFull, ok)) {
+          if (!*abort) fail();
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + C::kColO + 32 * ch, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tmem + lane_base + C::kColO + 32 * ch, o);
+        }
+      }
+      fence_proxy_async_smem();  // P is read by the tensor cores
+      tc_fence_before();
+      __syncwarp();  // the warp's P rows and O rescales are done
+      if (lane == 0) mbar_arrive(&p_full[b]);
+    }
+    // ---- the record: reference max, sum, unnormalised O of the row
+    if (__all_sync(kFull, *abort == 0)) {
+      const bool ok = wait_or_abort(o_done, (nstage - 1) & 1, abort);
+      if (__all_sync(kFull, ok)) {
+        tc_fence_after();
+        if (rv) write_record(m_used, l, -1, nullptr);
+#pragma unroll 1
+        for (int ch = 0; ch < D / 32; ++ch) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + C::kColO + 32 * ch, o);
+          if (rv) write_record(0.f, 0.f, ch, o);
+        }
+      } else if (!*abort) {
+        fail();
+      }
+    }
+  }
+
+  // ======================================================================== teardown
+  // every role is done: the issuer saw its MMAs complete, the producer its loads land
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D, bool FP8>
+cudaError_t launch_cascade_prefix_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p, dim3 grid,
+                                     cudaStream_t stream, int device) {
+  using C = TcPrefixCfg<D, FP8>;
+  auto kern = cascade_prefix_tc_kernel<D, FP8>;
+  static bool configured[64] = {};
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  if (!configured[device]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+    if (e != cudaSuccess) return e;
+    // tensor memory: the CTAs that can share an SM must not ask for more than its 512
+    // columns, or an allocation would wait for a CTA that cannot finish first
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kBytes);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1 || per_sm * C::kTmemCols > 512) return cudaErrorInvalidConfiguration;
+    configured[device] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+}
+
+#define PKV_DEFINE_PREFIX_TC(D, FP8)                                                                              \
+  template cudaError_t launch_cascade_prefix_tc<D, FP8>(const CUtensorMap&, const CUtensorMap&, const PrefixParams&, \
+                                                        dim3, cudaStream_t, int);
+PKV_DEFINE_PREFIX_TC(64, false)
+PKV_DEFINE_PREFIX_TC(128, false)
+PKV_DEFINE_PREFIX_TC(64, true)
+PKV_DEFINE_PREFIX_TC(128, true)
+#undef PKV_DEFINE_PREFIX_TC
+
+}  // namespace pkv

@@ -37,6 +37,9 @@
 
 namespace pkv {
 
+// Shared-prefix records a sequence's decode merges at most (splits of the prefix pass).
+constexpr int kMaxPrefixRecords = 16;
+
 struct DecodeParams {
   const uint16_t* q;            // [B][Hq][D] bf16
   const int32_t* block_tables;  // [B][max_blocks]

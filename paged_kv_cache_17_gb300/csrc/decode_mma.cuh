@@ -44,7 +44,10 @@ struct MmaCfg {
   static constexpr int kTilesBytes = kRingBytes;
   static constexpr int kBarOffset = kRingBytes + kConvBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 2 * STAGES * 8;  // 1024: alignment slack
-  static constexpr int kMergeBytes = NWC * (2 * G + G * D) * 4;
+  // merge scratch: the warps' states, then (cascade) the prefix records' (m, l) pairs and
+  // the weights of every part
+  static constexpr int kMergeBytes =
+      (NWC * (2 * G + G * D) + kMaxPrefixRecords * G * 2 + (NWC + kMaxPrefixRecords + 1) * G) * 4;
   static_assert(kMergeBytes <= kRingBytes, "merge scratch must fit in the tile ring");
   static_assert(G >= 1 && G <= 8, "a query group of at most 8 heads (the MMA's N)");
   static_assert(D == 64 || D == 128, "head_dim");
@@ -349,52 +352,103 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   const size_t out_row0 = static_cast<size_t>(b) * p.hq + hq0;
   const bool single = (nsplit == 1 && npre == 0);
   const bool with_prefix = CAS && (nsplit == 1 && npre > 0);
-  if (with_prefix) pdl_wait();
   const size_t prec0 = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots;
-  for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
-    const int g = e / D, d = e % D;
-    float M = -INFINITY;
+  if (CAS && with_prefix) {
+    // One partition plus the shared-prefix records: per head the total max over the warps
+    // and the records, each part's weight and the denominator (the records' (m, l) pairs
+    // come in one round trip), then per element the weighted sum with every record's
+    // output loaded independently of the others.
+    pdl_wait();
+    float* pml = aw + NWC * G * D;           // [npre][G][2] records' max and sum
+    float* wt = pml + kMaxPrefixRecords * G * 2;  // [NWC + npre][G] weights, then [G] 1 / denominator
+    for (int i = threadIdx.x; i < npre * G * 2; i += C::kThreads) pml[i] = __ldcg(&p.part_ml[prec0 * G * 2 + i]);
+    __syncthreads();
+    if (threadIdx.x < G) {
+      const int g = threadIdx.x;
+      float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NWC; ++w) M = fmaxf(M, mw[w * G + g]);
-    float num = 0.f, den = 0.f;
+      for (int w = 0; w < NWC; ++w) M = fmaxf(M, mw[w * G + g]);
+      for (int j = 0; j < npre; ++j) M = fmaxf(M, pml[(j * G + g) * 2]);
+      float den = 0.f;
+      if (M != -INFINITY) {
 #pragma unroll
-    for (int w = 0; w < NWC; ++w) {
-      const float wt = fast_exp2(mw[w * G + g] - M);  // warps without blocks: 2^-inf = 0
-      num = fmaf(wt, aw[(w * G + g) * D + d], num);
-      den = fmaf(wt, lw[w * G + g], den);
-    }
-    if constexpr (FP8) num *= 7.52316384526264e-37f;  // 2^-120: the E4M3 record units
-    if (CAS && with_prefix) {
-      float Mt = M;
-      for (int j = 0; j < npre; ++j) Mt = fmaxf(Mt, __ldcg(&p.part_ml[((prec0 + j) * G + g) * 2]));
-      float num2 = 0.f, den2 = 0.f;
-      if (Mt != -INFINITY) {
-        for (int j = 0; j < npre; ++j) {
-          const float wj = fast_exp2(__ldcg(&p.part_ml[((prec0 + j) * G + g) * 2]) - Mt);
-          num2 = fmaf(wj, __ldcg(&p.part_acc[((prec0 + j) * G + g) * D + d]), num2);
-          den2 = fmaf(wj, __ldcg(&p.part_ml[((prec0 + j) * G + g) * 2 + 1]), den2);
+        for (int w = 0; w < NWC; ++w) {
+          const float x = fast_exp2(mw[w * G + g] - M);  // warps without blocks: 0
+          wt[w * G + g] = x;
+          den = fmaf(x, lw[w * G + g], den);
         }
-        const float ws = fast_exp2(M - Mt);
-        num2 = fmaf(ws, num, num2);
-        den2 = fmaf(ws, den, den2);
+        for (int j = 0; j < npre; ++j) {
+          const float x = fast_exp2(pml[(j * G + g) * 2] - M);
+          wt[(NWC + j) * G + g] = x;
+          den = fmaf(x, pml[(j * G + g) * 2 + 1], den);
+        }
+      } else {
+        for (int w = 0; w < NWC + npre; ++w) wt[w * G + g] = 0.f;
       }
-      float ov = den2 > 0.f ? num2 / den2 : 0.f;
-      if constexpr (FP8) ov = (ov * 1152921504606846976.0f) * (p.scales[p.hkv + h] * 1152921504606846976.0f);
-      const size_t oi = (out_row0 + g) * D + d;
-      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = ov;
-      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov);
-    } else if (single) {
-      float ov = num / den;
-      if constexpr (FP8) ov = (ov * 1152921504606846976.0f) * (p.scales[p.hkv + h] * 1152921504606846976.0f);
-      const size_t oi = (out_row0 + g) * D + d;
-      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = ov;
-      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov);
-    } else {
-      const size_t rec = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots + p.pre_slots + s;
-      p.part_acc[(rec * G + g) * D + d] = num;
-      if (d == 0) {
-        p.part_ml[(rec * G + g) * 2 + 0] = M;
-        p.part_ml[(rec * G + g) * 2 + 1] = den;
+      wt[(NWC + npre) * G + g] = den > 0.f ? 1.f / den : 0.f;
+    }
+    __syncthreads();
+    constexpr int U = 4;  // elements per thread in flight
+    for (int e0 = threadIdx.x; e0 < G * D; e0 += U * C::kThreads) {
+      float num[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = e0 + u * C::kThreads;
+        num[u] = 0.f;
+        if (e < G * D) {
+          const int g = e / D, d = e % D;
+#pragma unroll
+          for (int w = 0; w < NWC; ++w) num[u] = fmaf(wt[w * G + g], aw[(w * G + g) * D + d], num[u]);
+          if constexpr (FP8) num[u] *= 7.52316384526264e-37f;  // 2^-120: the E4M3 record units
+        }
+      }
+      for (int j = 0; j < npre; ++j) {
+        const float* acc = p.part_acc + ((prec0 + j) * G) * D;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int e = e0 + u * C::kThreads;
+          if (e < G * D) num[u] = fmaf(wt[(NWC + j) * G + e / D], __ldcg(&acc[e]), num[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = e0 + u * C::kThreads;
+        if (e >= G * D) continue;
+        const int g = e / D;
+        float ov = num[u] * wt[(NWC + npre) * G + g];
+        if constexpr (FP8) ov = (ov * 1152921504606846976.0f) * (p.scales[p.hkv + h] * 1152921504606846976.0f);
+        const size_t oi = out_row0 * D + e;
+        if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = ov;
+        else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov);
+      }
+    }
+  } else {
+    for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
+      const int g = e / D, d = e % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NWC; ++w) M = fmaxf(M, mw[w * G + g]);
+      float num = 0.f, den = 0.f;
+#pragma unroll
+      for (int w = 0; w < NWC; ++w) {
+        const float wt = fast_exp2(mw[w * G + g] - M);  // warps without blocks: 2^-inf = 0
+        num = fmaf(wt, aw[(w * G + g) * D + d], num);
+        den = fmaf(wt, lw[w * G + g], den);
+      }
+      if constexpr (FP8) num *= 7.52316384526264e-37f;  // 2^-120: the E4M3 record units
+      if (single) {
+        float ov = num / den;
+        if constexpr (FP8) ov = (ov * 1152921504606846976.0f) * (p.scales[p.hkv + h] * 1152921504606846976.0f);
+        const size_t oi = (out_row0 + g) * D + d;
+        if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = ov;
+        else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(ov);
+      } else {
+        const size_t rec = prec0 + p.pre_slots + s;
+        p.part_acc[(rec * G + g) * D + d] = num;
+        if (d == 0) {
+          p.part_ml[(rec * G + g) * 2 + 0] = M;
+          p.part_ml[(rec * G + g) * 2 + 1] = den;
+        }
       }
     }
   }

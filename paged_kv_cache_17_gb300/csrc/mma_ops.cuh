@@ -77,6 +77,17 @@ __device__ __forceinline__ void split16(float a, float b, uint32_t& hi, uint32_t
   }
 }
 
+// sum of the two 16-bit values (bf16, or fp16 when F16) packed in w, in fp32 (exact widening)
+template <bool F16>
+__device__ __forceinline__ float sum16(uint32_t w) {
+  if constexpr (F16) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+    return f.x + f.y;
+  } else {
+    return __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+  }
+}
+
 // two E4M3 codes (low byte = first element) -> two fp16 values, exactly
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
   uint32_t r;

@@ -22,6 +22,7 @@ constexpr int kVersion = 100;  // 0.1.0
 constexpr int kMaxDevices = 64;
 constexpr int kMinSplitBlocks = 32;   // a context partition covers at least 512 tokens ...
 constexpr int kMaxSplitBlocks = 128;  // ... and at most 2048 (unless forced)
+constexpr int kMaxPrefixSlots = pkv::kMaxPrefixRecords;  // prefix-pass splits per prefix
 
 __device__ uint32_t g_pkv_status;  // PKV_DEVFLAG_* bits, one word per device
 
@@ -202,9 +203,11 @@ bool encode_kv_map_sw128(CUtensorMap* tm, void* base, int64_t num_blocks, int hk
 }
 
 // Splits of the prefix pass: each split is a run of whole 64-key stages (a multiple of four
-// blocks), at least two stages long; the count minimises (waves of CTAs, two resident per
-// SM) x (blocks per split + 8), the 8 blocks standing for a CTA's start-up and the merge
-// work every extra record adds; the fewest splits on a tie.
+// blocks), at least two stages long, at most kMaxPrefixRecords per prefix; the count
+// minimises (waves of CTAs, one resident per SM) x (blocks per split + 8), the 8 blocks
+// standing for a CTA's start-up and the merge work every extra record adds; the fewest
+// splits on a tie.  PKV_PREFIX_SPLIT_BLOCKS (>= 4) fixes the blocks per split, for tuning
+// and tests.
 struct PrefixPlan {
   int tiles;         // 64-row query tiles per prefix
   int pre_slots;     // splits per prefix
@@ -215,10 +218,21 @@ PrefixPlan plan_prefix(int num_prefixes, int max_members, int max_prefix_len, in
   PrefixPlan pp{0, 0, 0};
   const int pblocks = (max_prefix_len + 15) / 16;
   if (num_prefixes <= 0 || max_members <= 0 || pblocks <= 0) return pp;
-  pp.tiles = static_cast<int>((static_cast<long long>(max_members) * g + 63) / 64);
+  pp.tiles = static_cast<int>((static_cast<long long>(max_members) * g + 127) / 128);
   const long long per_split = static_cast<long long>(pp.tiles) * hkv * num_prefixes;
-  const long long slots = 2LL * sm_count;
-  const int max_splits = pblocks / 8 > 1 ? (pblocks / 8 < 16 ? pblocks / 8 : 16) : 1;
+  const long long slots = sm_count;  // one CTA per SM
+  if (const char* env = std::getenv("PKV_PREFIX_SPLIT_BLOCKS")) {  // tuning and tests: blocks per split
+    const long v = std::strtol(env, nullptr, 10);
+    if (v >= 4) {
+      long want = v < pblocks ? v : pblocks;
+      if (want * kMaxPrefixSlots < pblocks) want = (pblocks + kMaxPrefixSlots - 1) / kMaxPrefixSlots;
+      const int sb = static_cast<int>((want + 3) / 4 * 4);
+      pp.split_blocks = sb;
+      pp.pre_slots = (pblocks + sb - 1) / sb;
+      return pp;
+    }
+  }
+  const int max_splits = pblocks / 8 > 1 ? (pblocks / 8 < kMaxPrefixSlots ? pblocks / 8 : kMaxPrefixSlots) : 1;
   long long best_cost = -1;
   for (int n = 1; n <= max_splits; ++n) {
     const int sb = ((pblocks + n - 1) / n + 3) / 4 * 4;
@@ -616,11 +630,11 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (cache->head_dim == 64)
-    e = fp8 ? pkv::launch_cascade_prefix<64, true>(tk, tv, pr, pgrid, cs, device)
-            : pkv::launch_cascade_prefix<64, false>(tk, tv, pr, pgrid, cs, device);
+    e = fp8 ? pkv::launch_cascade_prefix_tc<64, true>(tk, tv, pr, pgrid, cs, device)
+            : pkv::launch_cascade_prefix_tc<64, false>(tk, tv, pr, pgrid, cs, device);
   else
-    e = fp8 ? pkv::launch_cascade_prefix<128, true>(tk, tv, pr, pgrid, cs, device)
-            : pkv::launch_cascade_prefix<128, false>(tk, tv, pr, pgrid, cs, device);
+    e = fp8 ? pkv::launch_cascade_prefix_tc<128, true>(tk, tv, pr, pgrid, cs, device)
+            : pkv::launch_cascade_prefix_tc<128, false>(tk, tv, pr, pgrid, cs, device);
   if (e != cudaSuccess) return cuda_fail(e, "prefix-pass launch");
   return decode_common(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, max_context_len,
                        softmax_scale, out, out_dtype, workspace, workspace_bytes, stream, px->seq_prefix,
