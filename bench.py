@@ -92,7 +92,7 @@ def step_bytes(w: W.Workload) -> dict:
 def decode_kernel_name(cfg, cascade: bool) -> str:
     """The kernels inside the decode call's timed interval (the merge runs only for split
     sequences)."""
-    tc = cfg.kv_dtype == "bf16" and os.environ.get("PKV_DECODE_CUDA_CORES") != "1"
+    tc = os.environ.get("PKV_DECODE_CUDA_CORES") != "1"  # both pool types run the tensor-core form
     core = "paged_decode_mma_kernel (tensor cores)" if tc else "paged_decode_kernel (CUDA cores)"
     name = core + " + merge_partitions_kernel"
     return ("cascade_prefix_tc_kernel (tcgen05) + " + name) if cascade else name
