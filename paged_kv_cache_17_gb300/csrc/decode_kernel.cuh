@@ -296,8 +296,19 @@ __device__ __forceinline__ void merge_records(const DecodeParams& p, int b, int 
 
 // CAS: the cascade variant, which merges shared-prefix records (seq_prefix, pre_slots);
 // the plain variant carries none of that code.
+// Register cap of the CUDA-core kernel: CTAs of NWC + 1 warps share an SM only while
+// ceil(n (NWC + 1) / 4) warps x regs x 32 fit one scheduler's 16K registers.  The G = 8,
+// D = 128 form aims at two CTAs per SM (168 registers; uncapped it takes 172 and drops to
+// one), every other form at three (128), which their shared memory allows.
+template <int D, int G, int NWC>
+struct DecodeRegCap {
+  static constexpr int kCtas = (D == 128 && G == 8) ? 2 : 3;
+  static constexpr int kWarpsPerScheduler = (kCtas * (NWC + 1) + 3) / 4;
+  static constexpr int kRegs = (16384 / (kWarpsPerScheduler * 32)) / 8 * 8;
+};
+
 template <int D, int G, bool FP8, int NWC, int STAGES, bool CAS>
-__global__ void __launch_bounds__((NWC + 1) * 32)
+__global__ void __launch_bounds__((NWC + 1) * 32) __maxnreg__((DecodeRegCap<D, G, NWC>::kRegs))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeParams p) {
   using C = DecodeCfg<D, G, FP8, NWC, STAGES>;
