@@ -59,6 +59,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--l2", choices=("flushed", "warm"), default="flushed",
+                    help="flushed (default): L2 flushed between timed steps; warm: no flush, a diagnostic of "
+                         "the reuse the shared-prefix and fork workloads get when a step follows a step")
     ap.add_argument("--no-clock-fill", action="store_true",
                     help="do not run the untimed clock-sampling loop when the timed region is too short "
                          "(for profiler runs)")
@@ -234,7 +237,8 @@ def oracle_sample(w: W.Workload, budget_s: float, threads: int):
     desc = (f"{'the whole step' if whole else f'{len(groups)} of {w.batch * c.hkv} (sequence, kv head) groups'}"
             f" x {reps} ({tok} tokens, {tok * per_tok / 1e6:.1f} MB of KV per pass), all {g} query heads of "
             f"each group; fp64 C oracle on {threads} threads")
-    return nbytes / dt / 1e9, dt, desc, nbytes
+    one_core = per_tok / max(sec_per_tok, 1e-12) / 1e9  # the first (sequence, kv head) group, one thread
+    return nbytes / dt / 1e9, dt, desc, nbytes, one_core
 
 
 def host_threads() -> int:
@@ -295,13 +299,20 @@ def run_ours(args):
             mark.record(stream)
         decode(t["q"], t["tables"], t["lens"])
 
+    cold = args.l2 == "flushed"
+
+    def evict(i):
+        if cold:
+            flush.fill_(i & 0xFF)  # evict the previous step's lines from L2 (not timed)
+
     def lead():
         # Untimed, between the L2 flush and the step: a read of a second buffer larger than
         # L2, which writes back the flush's dirty lines and leaves L2 holding clean, unrelated
         # lines (the timed kernel then pays for its own traffic only, as under ncu's cache
         # control), then a GPU spin long enough for this Python host loop to queue the whole
         # step before the GPU reaches it.
-        scrub.amax()
+        if cold:
+            scrub.amax()
         torch.cuda._sleep(HOST_LEAD_CYCLES)
 
     for _ in range(args.warmup):
@@ -320,14 +331,14 @@ def run_ours(args):
         # the step as a user runs it: append then decode, nothing in between (the decode's
         # launch overlaps the append's tail through programmatic dependent launch)
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)  # evict the previous step's lines from L2 (not timed)
+            evict(i)
             lead()
             evs[i][0].record(stream)
             step()
             evs[i][1].record(stream)
         # the decode kernel alone (the roofline figure): an event between append and decode
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            evict(i)
             lead()
             step(mark=dev_evs[i][0])
             dev_evs[i][1].record(stream)
@@ -410,7 +421,7 @@ def run_ours(args):
         ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+            evict(i)
             lead()  # untimed, as for the device timing: the copies and kernels stay inside
             ee[i][0].record(stream)
             e2e_step()
@@ -428,9 +439,9 @@ def run_ours(args):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         thr = host_threads()
-        gbs, dt, desc, _ = oracle_sample(w, args.cpu_seconds, thr)
+        gbs, dt, desc, _, one = oracle_sample(w, args.cpu_seconds, thr)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc,
-               "seconds": round(dt, 2)}
+               "seconds": round(dt, 2), "value_one_core": round(one, 4)}
     if ws > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
@@ -446,13 +457,15 @@ def run_ours(args):
                    "max_context_len": max_len, "total_context_tokens": w.total_tokens(),
                    "partition_tokens": pkv.partition_tokens(B, hkv, max_len),
                    "layout": args.layout, "decode_call": "cascade" if cas is not None else "paged",
-                   "l2": "flushed between timed steps: 256 MiB write, then a 256 MiB read of another buffer "
-                         "(both untimed; the read writes the dirty lines back before the step)",
+                   "l2": ("flushed between timed steps: 256 MiB write, then a 256 MiB read of another buffer "
+                          "(both untimed; the read writes the dirty lines back before the step)") if cold else
+                         "warm: no flush between steps (diagnostic; each step finds the previous step's lines)",
                    "parallelism": f"replicas x{ws}"},
         "us_per_step": round(ms_per_step * 1e3, 2),
         "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
         "bytes_per_step": nb,
         "decode_us": round(dec_avg_ms * 1e3, 2),
+        "decode_us_p10_p50_p90": [round(float(x) * 1e3, 2) for x in np.percentile(dec_ms, [10, 50, 90])],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None if cas is not None else ncu_traffic(cfg.name),
                      "kernel": decode_kernel_name(cfg, cas is not None),
@@ -608,7 +621,7 @@ def run_reference(args):
         oracle_sample(w, per_step, thr)
     total_b, total_s, desc = 0, 0.0, ""
     for _ in range(args.steps):
-        _, dt, desc, nbytes = oracle_sample(w, per_step, thr)
+        _, dt, desc, nbytes, _ = oracle_sample(w, per_step, thr)
         total_b += nbytes
         total_s += dt
     value = total_b / total_s / 1e9

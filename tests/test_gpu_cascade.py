@@ -167,3 +167,41 @@ def test_fp8_edge_cases(pkv, d):
     ref = oracle.decode_all(W.bf16_bits(q), k8.numpy(), v8.numpy(), oracle.KV_E4M3, full.numpy(), lens.numpy(),
                             scale, scales=scales.numpy())
     assert_close(out.cpu().double().numpy(), ref, "fp8", f"cascade fp8 edges d={d}")
+
+
+def test_cascade_shared_prefix_bitwise_consistent(pkv):
+    """The shared-prefix workload's consistency variant through the cascade call: the same q
+    for every member gives identical output bits (ml-canon.vercel.app/54-prefix-caching-cacheblend.html,
+    "Идея и механизм": the prefix KV is identical across requests), with no own blocks and
+    with bit-equal own blocks; members 0 and 200 sit in different 128-row tiles of the
+    prefix pass."""
+    w = W.make_workload("prefix_shared")
+    t = to_dev(w)
+    c = w.cascade()
+    B = w.batch
+    q = t["q"][:1].expand(B, -1, -1).contiguous()
+    dev = q.device
+    args = dict(max_members=c.max_members, max_prefix_len=c.max_prefix_len)
+
+    def run(lens):
+        out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        pkv.cascade_decode_attention(q, t["k_cache"], t["v_cache"], c.prefix_tables.to(dev), c.prefix_lens.to(dev),
+                                     c.member_indptr.to(dev), c.member_seqs.to(dev), c.seq_prefix.to(dev),
+                                     c.block_tables.to(dev), lens.to(dev), w.cfg.softmax_scale, out,
+                                     max_context_len=max(16, int(lens.max())), **args)
+        torch.cuda.synchronize()
+        assert pkv.check_device_status() == 0
+        return out
+
+    out = run(torch.zeros_like(c.context_lens))
+    assert all(torch.equal(out[0], out[i]) for i in range(1, B)), "prefix-only outputs differ"
+    b0, b1 = 0, 200
+    lens = c.context_lens.clone()
+    n = int(min(lens[b0], lens[b1]))
+    lens[b0] = lens[b1] = n
+    for j in range((n + 15) // 16):
+        src, dst = int(c.block_tables[b0, j]), int(c.block_tables[b1, j])
+        t["k_cache"][dst] = t["k_cache"][src]
+        t["v_cache"][dst] = t["v_cache"][src]
+    out2 = run(lens)
+    assert torch.equal(out2[b0], out2[b1]), "equal suffixes, different bits"
