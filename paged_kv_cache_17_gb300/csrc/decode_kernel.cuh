@@ -337,6 +337,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32) __maxnreg__((DecodeRegCap<D, G
 
   // ---- sequence length (checked, clamped) and this CTA's share of it
   int len = p.context_lens[b];
+  // the first 32 block ids of this partition, loaded beside the length (the row has
+  // max_blocks valid entries; ids past the context are never used or checked)
+  const int blk0 = s * p.split_blocks;
+  const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk0;
+  int ids = (warp == NWC && blk0 + lane < p.max_blocks) ? row[lane] : 0;
   {
     const int cap = min(p.max_context_len, p.max_blocks * kBlockSize);
     if (len < 0 || len > cap) {
@@ -371,12 +376,9 @@ __global__ void __launch_bounds__((NWC + 1) * 32) __maxnreg__((DecodeRegCap<D, G
     if constexpr (CAS) pdl_wait();
     return;
   }
-  const int blk0 = s * p.split_blocks;
   const int nloc = min(nblk, blk0 + p.split_blocks) - blk0;
 
   // issue the first global loads now, so their latency overlaps the barrier set-up
-  const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk0;
-  int ids = (warp == NWC && lane < nloc) ? row[lane] : 0;
   const int hg = warp % HG;  // head group of a consumer warp
   uint32_t qbits[GW][DPL / 2];
   if (warp < NWC) {

@@ -79,6 +79,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   if constexpr (!CAS) pdl_wait();
 
   int len = p.context_lens[b];
+  // the first 32 block ids of this partition, loaded beside the length (the row has
+  // max_blocks valid entries; ids past the context are never used or checked)
+  const int blk0 = s * p.split_blocks;
+  const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk0;
+  int ids = (warp == NWC && blk0 + lane < p.max_blocks) ? row[lane] : 0;
   {
     const int cap = min(p.max_context_len, p.max_blocks * kBlockSize);
     if (len < 0 || len > cap) {
@@ -111,11 +116,8 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
     if constexpr (CAS) pdl_wait();
     return;
   }
-  const int blk0 = s * p.split_blocks;
   const int nloc = min(nblk, blk0 + p.split_blocks) - blk0;
 
-  const int32_t* row = p.block_tables + static_cast<size_t>(b) * p.max_blocks + blk0;
-  int ids = (warp == NWC && lane < nloc) ? row[lane] : 0;
   // q as the B operand of the score product: column n = head gid of the group (zero
   // columns past G), k = head_dim; one pair of bf16 words per k-step
   uint32_t qb[KS][2];
