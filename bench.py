@@ -68,6 +68,16 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest of every rank's x (timings: the job is as slow as its slowest rank); one
+    all-reduce outside the data path, and nothing to do for a single rank."""
+    if ws <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -364,10 +374,7 @@ def run_ours(args):
     step_ms = [a.elapsed_time(b) for (a, b) in evs]
     dec_ms = [a.elapsed_time(b) for (a, b) in dev_evs]
     tot_ms = sum(step_ms)
-    if ws > 1:
-        tt = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        tot_ms = float(tt.item())
+    tot_ms = max_over_ranks(tot_ms, ws, dev)
     assert pkv.check_device_status() == 0
     value = nb["step"] * ws * args.steps / (tot_ms * 1e-3) / 1e9
     ms_per_step = tot_ms / args.steps
@@ -428,10 +435,7 @@ def run_ours(args):
             ee[i][1].record(stream)
         torch.cuda.synchronize()
         e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
-        if ws > 1:
-            tt = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(e2e_ms, ws, dev)
         e2e = {"value": round(nb["step"] * ws * args.steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e2e_ms / args.steps, 4)}
@@ -553,10 +557,7 @@ def run_copy_blocks(args):
     clocks = clk.summary()
     clocks["window"] = "timed region"
     tot_ms = sum(a.elapsed_time(b) for a, b in evs)
-    if ws > 1:
-        tt = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        tot_ms = float(tt.item())
+    tot_ms = max_over_ranks(tot_ms, ws, dev)
     assert pkv.check_device_status() == 0
     achieved = moved * args.steps / (tot_ms * 1e-3) / 1e9
     # end to end: the pair list comes from pinned host memory every step
