@@ -504,13 +504,18 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
         if constexpr (C::kPSplit) st_shared_v4(plrow + ((c ^ (r & 7)) << 4), wl[0], wl[1], wl[2], wl[3]);
       }
       l += ls;
-      // rescale O where this warp's rows moved their reference max (after O += P V of t - 1)
-      if (t > 0 && __any_sync(kFull, grow)) {
+      // O += P V of stage t - 1 is done.  Waited at every stage, rescale or not: a parity
+      // wait is unambiguous only while the barrier is at most one phase past the waiter,
+      // and O += P V of stage t cannot start before this warp's arrival below
+      if (t > 0) {
         ok = wait_or_abort(o_done, (t - 1) & 1, abort);
         if (!__all_sync(kFull, ok)) {
           if (!*abort) fail();
           break;
         }
+      }
+      // rescale O where this warp's rows moved their reference max
+      if (t > 0 && __any_sync(kFull, grow)) {
         tc_fence_after();
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
@@ -526,7 +531,8 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
       __syncwarp();  // the warp's P rows and O rescales are done
       if (lane == 0) mbar_arrive(&p_full[b]);
     }
-    // ---- the record: reference max, sum, unnormalised O of the row
+    // ---- the record: reference max, sum, unnormalised O of the row (the stages before the
+    // last were waited in the loop, so the barrier is at the last phase or one past it)
     if (__all_sync(kFull, *abort == 0)) {
       const bool ok = wait_or_abort(o_done, (nstage - 1) & 1, abort);
       if (__all_sync(kFull, ok)) {
