@@ -120,7 +120,8 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
   uint64_t* p_full = s_full + 2;     // [2] P of a stage written (one arrival per softmax warp)
   uint64_t* o_done = p_full + 2;     // O += P V of a stage done
   uint64_t* drain = o_done + 1;      // every MMA issued so far done (abort path)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* q_full = drain + 1;      // Q staged (one arrival per softmax warp)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tile = blockIdx.x;
@@ -134,7 +135,9 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
   // grid (the pool after the append) is complete once every CTA is past the wait above
   pdl_launch_dependents();
 
+  // one round trip: the member range and the prefix length
   const int m0 = p.indptr[pfx], m1 = p.indptr[pfx + 1];
+  int plen = p.prefix_lens[pfx];
   int members = m1 - m0;
   if (members < 0 || members > p.max_members) {  // the grid covers max_members members
     if (threadIdx.x == 0 && tile == 0 && split == 0 && h == 0) set_flag(p.status, PKV_DEVFLAG_BAD_CONTEXT_LEN);
@@ -143,7 +146,6 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
   const int G = p.group;
   const int rows = members * G;
   if (tile * C::kRows >= rows) return;
-  int plen = p.prefix_lens[pfx];
   if (plen < 0 || plen > p.max_prefix_blocks * kBlockSize || (plen & (kBlockSize - 1))) {
     if (threadIdx.x == 0 && tile == 0 && split == 0 && h == 0) set_flag(p.status, PKV_DEVFLAG_BAD_CONTEXT_LEN);
     plen = max(0, min(plen, p.max_prefix_blocks * kBlockSize)) & ~(kBlockSize - 1);
@@ -159,7 +161,8 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
   const int r = threadIdx.x;  // softmax threads: row r of the tile, TMEM lane r
   bool rv = false;
   int rb = 0, rg = 0;
-  if (soft) {
+  // the row's sequence (softmax threads; a global load, issued once the setup below is done)
+  auto load_row = [&]() {
     const int row = tile * C::kRows + r;
     rv = row < rows;
     if (rv) {
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
         rb = 0;
       }
     }
-  }
+  };
   const float vunit = FP8 ? 7.52316384526264e-37f : 1.0f;  // 2^-120: the decode kernel's E4M3 units
   auto write_record = [&](float m, float l, int chunk, const float* o32) {
     // chunk < 0: m and l; else 32 output columns starting at 32 * chunk
@@ -189,6 +192,7 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
     }
   };
   if (nstage == 0) {  // an empty split: m = -inf, l = 0, o = 0
+    if (soft) load_row();
     if (soft && rv) {
       float z[32];
 #pragma unroll
@@ -200,24 +204,6 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
     return;
   }
 
-  // ---- Q rows -> shared memory, K-major 128-byte swizzle (16-bit; fp16 for E4M3 pools)
-  const uint32_t q_base = smem_u32(smem + C::kOffQ);
-  if (soft) {
-    const uint4* qr = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(rb) * p.hq + h * G + rg) * D);
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      uint4 v = rv ? qr[c] : make_uint4(0u, 0u, 0u, 0u);
-      if constexpr (FP8) {
-        v.x = pack_f16(bf16_lo(v.x), bf16_hi(v.x));
-        v.y = pack_f16(bf16_lo(v.y), bf16_hi(v.y));
-        v.z = pack_f16(bf16_lo(v.z), bf16_hi(v.z));
-        v.w = pack_f16(bf16_lo(v.w), bf16_hi(v.w));
-      }
-      st_shared_v4(q_base + (c >> 3) * C::kQHalf + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4), v.x,
-                   v.y, v.z, v.w);
-    }
-    fence_proxy_async_smem();  // read by the tensor cores
-  }
   if (warp == 0) {
     __syncwarp();
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -239,15 +225,40 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
     }
     mbar_init(o_done, 1);
     mbar_init(drain, 1);
+    mbar_init(q_full, C::kSoftWarps);
     *abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
   }
+  // the setup above reads no global memory, so the producer's first loads start one round
+  // trip after the launch; the softmax warps stage Q meanwhile
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // ---- Q rows -> shared memory, K-major 128-byte swizzle (16-bit; fp16 for E4M3 pools)
+  const uint32_t q_base = smem_u32(smem + C::kOffQ);
+  if (soft) {
+    load_row();
+    const uint4* qr = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(rb) * p.hq + h * G + rg) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      uint4 v = rv ? qr[c] : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (FP8) {
+        v.x = pack_f16(bf16_lo(v.x), bf16_hi(v.x));
+        v.y = pack_f16(bf16_lo(v.y), bf16_hi(v.y));
+        v.z = pack_f16(bf16_lo(v.z), bf16_hi(v.z));
+        v.w = pack_f16(bf16_lo(v.w), bf16_hi(v.w));
+      }
+      st_shared_v4(q_base + (c >> 3) * C::kQHalf + (r >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4), v.x,
+                   v.y, v.z, v.w);
+    }
+    fence_proxy_async_smem();  // read by the tensor cores
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q_full);
+  }
 
   auto fail = [&]() {
     set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
@@ -326,7 +337,7 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
         if constexpr (FP8) return wait_or_abort(&exp_full[t % E], (t / E) & 1, abort);
         return wait_or_abort(&full[t % R], (t / R) & 1, abort);
       };
-      bool ok = true;
+      bool ok = wait_or_abort(q_full, 0, abort);  // Q staged by the softmax warps
       for (int t = 0; t < min(2, nstage) && ok; ++t) {
         ok = wait_tiles(t);
         if (ok) issue_s(t);
