@@ -36,9 +36,12 @@ struct PrefixParams {
 // bf16 pools are read through the 128-byte-swizzled 64-column tensor maps, E4M3 pools
 // through the plain ones.
 template <int D, bool FP8>
+int cascade_prefix_tc_ctas_per_sm(int device);  // CTAs of the pass resident per SM; 0 on error
+template <int D, bool FP8>
 cudaError_t launch_cascade_prefix_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p, dim3 grid,
                                      cudaStream_t stream, int device);
 #define PKV_DECLARE_PREFIX_TC(D, FP8)                                                                        \
+  extern template int cascade_prefix_tc_ctas_per_sm<D, FP8>(int);                                           \
   extern template cudaError_t launch_cascade_prefix_tc<D, FP8>(const CUtensorMap&, const CUtensorMap&,      \
                                                                const PrefixParams&, dim3, cudaStream_t, int);
 PKV_DECLARE_PREFIX_TC(64, false)

@@ -14,31 +14,38 @@
 //
 //   S [128 rows x 64 keys] = Q [128 x D] K^T          (tcgen05.mma kind::f16, fp32 in TMEM)
 //   P = 2^(S * scale - m)                             (one thread per row, CUDA cores)
-//   O [128 x D]          += P [128 x 64] V [64 x D]   (O stays in TMEM for the whole split)
+//   O [128 x D]          += P [128 x 64] V [64 x D]   (P read from TMEM; O stays in TMEM)
 //
 // CTA = 128 query rows (row r: member r / G, query head h * G + r % G), one kv head, one
 // split of the prefix (a run of whole 64-key stages):
 //   warps 0-3  softmax: thread r owns row r (TMEM lane r); reads S, writes P as 16-bit
-//              values into the stage's K tile (K is no longer needed once S is computed),
-//              rescales its O row when its reference max moved, and writes the record;
-//              bf16 pools write P as bf16 hi + lo (lo = P - hi rounded, in a buffer of its
-//              own), and O += P V runs once for each, so the weights keep about 16 bits;
+//              pairs back over the stage's own S columns, rescales its O row when its
+//              reference max moved, and writes the record; bf16 pools write P as bf16
+//              hi + lo (lo = P - hi rounded) and O += P V runs once for each, so the weights
+//              keep about 16 bits;
 //   warp 4     lane 0 issues every MMA;
 //   warp 5     the producer: block ids of the split 32 at a time in its lanes, one TMA box
-//              per (block, 64 columns, K or V) into the ring as slots come free;
-//   warps 6-9  (E4M3 pools) expand each raw stage exactly to fp16 into a 16-bit ring.
+//              per (block, 64 columns) into the K and V rings as slots come free;
+//   warps 6-9  (E4M3 pools) expand each raw stage exactly to fp16 into 16-bit rings.
 // S is double-buffered in TMEM, so the tensor cores compute S of stage t + 2 and O of stage
-// t while the softmax warps work on stage t + 1.  The reference max of a row changes only
-// when the row max exceeds it by more than 2^8 (weights then stay <= 256, exact in bf16 and
-// fp16 range), so O is rescaled rarely; the record carries the reference max it used.
+// t while the softmax warps work on stage t + 1.  K and V have rings of their own: a K
+// slot is free once S of its stage is done, long before O += P V of that stage, so K of
+// stage t + 2 is loaded while stage t is still being weighed.  The reference max of a row
+// changes only when the row max exceeds it by more than 2^8 (weights then stay <= 256,
+// exact in bf16 and fp16 range), so O is rescaled rarely; the record carries the reference
+// max it used.
 //
-// Shared memory: Q (128 x D, 16-bit, 128-byte swizzled, K-major), a 4-stage TMA ring of K
-// and V tiles ([column half][64 keys][128 bytes], swizzled by the TMA load), for E4M3 a
-// 3-stage ring of expanded fp16 tiles; D = 64 gives P two buffers of its own, bf16 pools
-// two more for the lo parts.  TMEM: S at
-// columns 0 and 64, O at column 128 (256 columns; one or two CTAs per SM).
+// Each CTA is one chain of dependent steps (S -> weights -> O += P V) whose latency, not
+// any one unit's throughput, sets its pace; so two CTAs fit on an SM (shared memory at most
+// 98 KiB and 256 TMEM columns each) and their chains interleave.
+// Shared memory: Q (128 x D, 16-bit, 128-byte swizzled, K-major) and K and V rings ([column
+// half][64 keys][128 bytes], swizzled by the TMA load; 2 stages each at D = 128, 4 at
+// D = 64); E4M3 pools add rings of expanded fp16 tiles (1 stage each at D = 128, 2 at
+// D = 64).  TMEM: S (then P) at columns 0 and 64, O at column 128.
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "cascade.cuh"
 #include "mma_ops.cuh"
@@ -52,34 +59,35 @@ struct TcPrefixCfg {
   static constexpr int kRows = 128;             // query rows per CTA: the MMA's M
   static constexpr int kKeys = 64;              // keys per stage: N of S, K of O += P V
   static constexpr int kStageBlocks = kKeys / kBlockSize;
-  static constexpr int kRing = 4;               // TMA ring depth
-  static constexpr int kExp = 3;                // E4M3: expanded 16-bit stages
+  // stages per K ring and per V ring as loaded, and per ring of expanded 16-bit E4M3 tiles:
+  // as deep as two CTAs per SM allow
+  static constexpr int kRing = D == 64 ? 4 : 2;
+  static constexpr int kExpRing = D == 64 ? 2 : 1;
   static constexpr int kHalves = D / 64;
   static constexpr int kQHalf = kRows * 128;    // one 64-column half of Q
   static constexpr int kHalf16 = kKeys * 128;   // one 64-column half of a 16-bit K or V stage
   static constexpr int kTile16 = kHalves * kHalf16;
   static constexpr int kRaw = FP8 ? kKeys * D : kTile16;  // a K or V stage as loaded
-  static constexpr int kPBytes = kRows * kKeys * 2;
-  static constexpr bool kPInK = kTile16 >= kPBytes;
   static constexpr bool kPSplit = !FP8;         // bf16 weights as hi + lo (two P V products)
-  static constexpr int kPBufs = (kPInK ? 0 : 2) + (kPSplit ? 2 : 0);
   static constexpr int kOffQ = 0;
   static constexpr int kOffRawK = kOffQ + kHalves * kQHalf;
   static constexpr int kOffRawV = kOffRawK + kRing * kRaw;
   static constexpr int kOffExpK = kOffRawV + kRing * kRaw;
-  static constexpr int kOffExpV = kOffExpK + (FP8 ? kExp * kTile16 : 0);
-  static constexpr int kOffP = kOffExpV + (FP8 ? kExp * kTile16 : 0);
-  static constexpr int kOffBar = kOffP + kPBufs * kPBytes;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kOffExpV = kOffExpK + (FP8 ? kExpRing * kTile16 : 0);
+  static constexpr int kOffBar = kOffExpV + (FP8 ? kExpRing * kTile16 : 0);
+  static constexpr int kBarBytes = 512;
   static constexpr int kBytes = 1024 + kOffBar + kBarBytes;  // 1024: alignment slack
   static constexpr int kColS = 0, kColO = 128, kTmemCols = 256;
   static constexpr int kSoftWarps = 4, kIssuerWarp = 4, kProducerWarp = 5, kConvWarp0 = 6;
   static constexpr int kConvWarps = FP8 ? 4 : 0;
   static constexpr int kThreads = (kConvWarp0 + kConvWarps) * 32;
+  static constexpr int kMinCtas = 2;            // CTAs per SM the registers are capped for
   static constexpr float kLazy = 8.f;           // log2 of the largest weight before a rescale
   static_assert(D == 64 || D == 128, "head_dim");
-  static_assert(kRaw % 1024 == 0 && kTile16 % 1024 == 0 && kPBytes % 1024 == 0, "1024-byte aligned tiles");
+  static_assert(kRaw % 1024 == 0 && kTile16 % 1024 == 0, "1024-byte aligned tiles");
   static_assert(kColO + D <= kTmemCols, "TMEM columns");
+  static_assert(2 * (kBytes + 1024) <= 228 * 1024, "two CTAs per SM");
+  static_assert((8 * kRing + 7) * 8 + 8 <= kBarBytes, "barriers, TMEM address and abort flag");
 };
 
 namespace {
@@ -104,23 +112,26 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }  // namespace
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
+__global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, TcPrefixCfg<D, FP8>::kMinCtas)
     cascade_prefix_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                              const PrefixParams p) {
   using C = TcPrefixCfg<D, FP8>;
-  constexpr int R = C::kRing, E = C::kExp;
+  constexpr int R = C::kRing, E = C::kExpRing;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kOffBar);  // [R] TMA landed
-  uint64_t* empty = full + R;        // [R] bf16: O += P V of the slot's stage done
-  uint64_t* raw_empty = empty + R;   // [R] E4M3: the slot's raw stage expanded
-  uint64_t* exp_full = raw_empty + R;  // [E] E4M3: stage expanded
-  uint64_t* exp_empty = exp_full + E;  // [E] E4M3: O += P V of the slot's stage done
-  uint64_t* s_full = exp_empty + E;  // [2] S of a stage done
-  uint64_t* p_full = s_full + 2;     // [2] P of a stage written (one arrival per softmax warp)
-  uint64_t* o_done = p_full + 2;     // O += P V of a stage done
-  uint64_t* drain = o_done + 1;      // every MMA issued so far done (abort path)
-  uint64_t* q_full = drain + 1;      // Q staged (one arrival per softmax warp)
+  uint64_t* kfull = reinterpret_cast<uint64_t*>(smem + C::kOffBar);  // [R] K stage landed (TMA)
+  uint64_t* vfull = kfull + R;    // [R] V stage landed
+  uint64_t* kfree = vfull + R;    // [R] K slot reusable: bf16 S of its stage done, E4M3 expanded
+  uint64_t* vfree = kfree + R;    // [R] V slot reusable: bf16 O += P V of its stage done, E4M3 expanded
+  uint64_t* ekfull = vfree + R;   // [R] E4M3: K stage expanded
+  uint64_t* evfull = ekfull + R;  // [R] E4M3: V stage expanded
+  uint64_t* ekfree = evfull + R;  // [R] E4M3: S of the expanded slot's stage done
+  uint64_t* evfree = ekfree + R;  // [R] E4M3: O += P V of the expanded slot's stage done
+  uint64_t* s_full = evfree + R;  // [2] S of a stage done
+  uint64_t* p_full = s_full + 2;  // [2] P of a stage written (one arrival per softmax warp)
+  uint64_t* o_done = p_full + 2;  // O += P V of a stage done
+  uint64_t* drain = o_done + 1;   // every MMA issued so far done (abort path)
+  uint64_t* q_full = drain + 1;   // Q staged (one arrival per softmax warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_full + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -211,13 +222,14 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
   }
   if (threadIdx.x == C::kIssuerWarp * 32) {
     for (int i = 0; i < R; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-      mbar_init(&raw_empty[i], 1);
-    }
-    for (int i = 0; i < E; ++i) {
-      mbar_init(&exp_full[i], 1);
-      mbar_init(&exp_empty[i], 1);
+      mbar_init(&kfull[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&kfree[i], 1);
+      mbar_init(&vfree[i], 1);
+      mbar_init(&ekfull[i], 1);
+      mbar_init(&evfull[i], 1);
+      mbar_init(&ekfree[i], 1);
+      mbar_init(&evfree[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -264,42 +276,12 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
     set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
     *abort = 1;
   };
-  // TMA of stage t into ring slot t % R: block j of the stage starts at pool row row0[j]
-  // (-16 for blocks past the split: a box entirely outside the tensor reads zeros)
-  auto tma_stage = [&](int t, const int (&row0)[C::kStageBlocks]) {
-    const int st = t % R;
-    mbar_arrive_expect_tx(&full[st], 2 * C::kRaw);
-#pragma unroll
-    for (int j = 0; j < C::kStageBlocks; ++j) {
-      if constexpr (FP8) {
-        const int off = st * C::kRaw + j * kBlockSize * D;
-        tma_load_3d(smem + C::kOffRawK + off, &tm_k, 0, h, row0[j], &full[st]);
-        tma_load_3d(smem + C::kOffRawV + off, &tm_v, 0, h, row0[j], &full[st]);
-      } else {
-#pragma unroll
-        for (int hf = 0; hf < C::kHalves; ++hf) {
-          const int off = st * C::kRaw + hf * C::kHalf16 + j * 2048;
-          tma_load_3d(smem + C::kOffRawK + off, &tm_k, hf * 64, h, row0[j], &full[st]);
-          tma_load_3d(smem + C::kOffRawV + off, &tm_v, hf * 64, h, row0[j], &full[st]);
-        }
-      }
-    }
-  };
-  // the 16-bit K and V tiles and the P buffer of stage t
+  // the 16-bit K and V tiles of stage t (the raw slots, or for E4M3 the expanded ones)
   auto k_tile = [&](int t) -> uint32_t {
     return FP8 ? smem_u32(smem + C::kOffExpK + (t % E) * C::kTile16) : smem_u32(smem + C::kOffRawK + (t % R) * C::kRaw);
   };
   auto v_tile = [&](int t) -> uint32_t {
     return FP8 ? smem_u32(smem + C::kOffExpV + (t % E) * C::kTile16) : smem_u32(smem + C::kOffRawV + (t % R) * C::kRaw);
-  };
-  // P (or its hi part) of stage t: the stage's K tile, else one of two buffers; the lo part
-  // of bf16 weights: two buffers after those (a buffer is rewritten two stages later, when
-  // S of that stage is done, which implies O += P V of this stage is done)
-  auto p_tile = [&](int t) -> uint32_t {
-    return C::kPInK ? k_tile(t) : smem_u32(smem + C::kOffP + (t & 1) * C::kPBytes);
-  };
-  auto plo_tile = [&](int t) -> uint32_t {
-    return smem_u32(smem + C::kOffP + ((C::kPInK ? 0 : 2) + (t & 1)) * C::kPBytes);
   };
 
   if (warp == C::kIssuerWarp) {
@@ -307,7 +289,7 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_f16(C::kRows, C::kKeys, !FP8, false);
       constexpr uint32_t kIdO = idesc_f16(C::kRows, D, !FP8, true);
-      // S(t) into buffer t % 2: D/16 k-steps of 16 head dims (byte 32k of a 128-byte row)
+      // S(t) into TMEM buffer t % 2: D/16 k-steps of 16 head dims (byte 32k of a 128-byte row)
       auto issue_s = [&](int t) {
         const uint32_t kt = k_tile(t);
         tc_fence_after();
@@ -318,36 +300,41 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
           mma_f16_ss(tmem + C::kColS + 64 * (t & 1), a, b, kIdS, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[t & 1]);
+        tc_commit(FP8 ? &ekfree[t % E] : &kfree[t % R]);  // the K tile is read
       };
-      // O += P(t) V(t): 4 k-steps of 16 keys; V is MN-major (64 head dims per 128-byte row)
+      // O += P(t) V(t): 4 k-steps of 16 keys; P (the A operand) in TMEM over the S columns of
+      // stage t (hi at +0, lo at +32, two weights per column); V is MN-major (64 head dims per
+      // 128-byte row).  The MMAs run in issue order, so S(t + 2), issued after these into the
+      // same columns, overwrites P(t) only once these have read it.
       auto issue_o = [&](int t) {
-        const uint32_t pt = p_tile(t), vt = v_tile(t);
+        const uint32_t pt = tmem + C::kColS + 64 * (t & 1), vt = v_tile(t);
         tc_fence_after();
 #pragma unroll
         for (int j = 0; j < C::kKeys / 16; ++j) {
-          const uint64_t a = sdesc_sw128(pt + j * 32, 16, 1024);
           const uint64_t b = sdesc_sw128(vt + j * 2048, C::kHalf16, 1024);
-          mma_f16_ss(tmem + C::kColO, a, b, kIdO, (t > 0 || j > 0) ? 1u : 0u);
-          if constexpr (C::kPSplit) mma_f16_ss(tmem + C::kColO, sdesc_sw128(plo_tile(t) + j * 32, 16, 1024), b, kIdO, 1u);
+          mma_f16_ts(tmem + C::kColO, pt + 8 * j, b, kIdO, (t > 0 || j > 0) ? 1u : 0u);
+          if constexpr (C::kPSplit) mma_f16_ts(tmem + C::kColO, pt + 32 + 8 * j, b, kIdO, 1u);
         }
-        tc_commit(FP8 ? &exp_empty[t % E] : &empty[t % R]);
+        tc_commit(FP8 ? &evfree[t % E] : &vfree[t % R]);  // the V tile is read
         tc_commit(o_done);
       };
-      auto wait_tiles = [&](int t) -> bool {
-        if constexpr (FP8) return wait_or_abort(&exp_full[t % E], (t / E) & 1, abort);
-        return wait_or_abort(&full[t % R], (t / R) & 1, abort);
+      auto wait_k = [&](int t) -> bool {
+        return FP8 ? wait_or_abort(&ekfull[t % E], (t / E) & 1, abort) : wait_or_abort(&kfull[t % R], (t / R) & 1, abort);
+      };
+      auto wait_v = [&](int t) -> bool {
+        return FP8 ? wait_or_abort(&evfull[t % E], (t / E) & 1, abort) : wait_or_abort(&vfull[t % R], (t / R) & 1, abort);
       };
       bool ok = wait_or_abort(q_full, 0, abort);  // Q staged by the softmax warps
       for (int t = 0; t < min(2, nstage) && ok; ++t) {
-        ok = wait_tiles(t);
+        ok = wait_k(t);
         if (ok) issue_s(t);
       }
       for (int t = 0; t < nstage && ok; ++t) {
-        ok = wait_or_abort(&p_full[t & 1], (t >> 1) & 1, abort);
+        ok = wait_or_abort(&p_full[t & 1], (t >> 1) & 1, abort) && wait_v(t);
         if (!ok) break;
         issue_o(t);
         if (t + 2 < nstage) {
-          ok = wait_tiles(t + 2);
+          ok = wait_k(t + 2);
           if (!ok) break;
           issue_s(t + 2);
         }
@@ -360,28 +347,21 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
     __syncwarp();
   } else if (warp == C::kProducerWarp) {
     // ======================================================================== TMA producer
-    // block ids of the split, 32 (eight stages) at a time in the lanes, the next 32 in flight
+    // block ids of the split, 32 (eight stages) at a time in the lanes, the next 32 in flight;
+    // K of stage t + 1 goes before V of stage t (its slot frees earlier: when S of stage
+    // t - 1 is done, before O += P V of stage t - 2)
     const int nblk = blk1 - blk0;
     int ids = lane < nblk ? table[blk0 + lane] : 0;
     int nxt = 32 + lane < nblk ? table[blk0 + 32 + lane] : 0;
-    int issued = 0;
-    bool ok = true;
-    for (int t = 0; t < nstage; ++t) {
-      const int st = t % R;
-      if (t >= R) {  // the slot's previous stage is consumed
-        ok = wait_or_abort(FP8 ? &raw_empty[st] : &empty[st], ((t / R) - 1) & 1, abort);
-        if (!__all_sync(kFull, ok)) {
-          ok = false;
-          break;
-        }
-      }
+    // pool rows of the blocks of stage t (called for t = 0, 1, 2, ... in order); -16 for
+    // blocks past the split: a box entirely outside the tensor reads zeros
+    auto stage_rows = [&](int t, int (&row0)[C::kStageBlocks]) {
       const int w0 = (t * C::kStageBlocks) & 31;
       if (t > 0 && w0 == 0) {
         ids = nxt;
         const int k = t * C::kStageBlocks + 32 + lane;
         nxt = k < nblk ? table[blk0 + k] : 0;
       }
-      int row0[C::kStageBlocks];
 #pragma unroll
       for (int j = 0; j < C::kStageBlocks; ++j) {
         const int pb = __shfl_sync(kFull, ids, w0 + j);
@@ -391,14 +371,60 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
           else if (lane == 0) set_flag(p.status, PKV_DEVFLAG_BAD_BLOCK_ID);
         }
       }
-      if (lane == 0) tma_stage(t, row0);
-      issued = t + 1;
+    };
+    // TMA of one tensor's stage t into ring slot t % R (lane 0)
+    auto load = [&](const CUtensorMap* tm, int off_ring, uint64_t* bar, const int (&row0)[C::kStageBlocks], int t) {
+      const int st = t % R;
+      mbar_arrive_expect_tx(&bar[st], C::kRaw);
+#pragma unroll
+      for (int j = 0; j < C::kStageBlocks; ++j) {
+        if constexpr (FP8) {
+          tma_load_3d(smem + off_ring + st * C::kRaw + j * kBlockSize * D, tm, 0, h, row0[j], &bar[st]);
+        } else {
+#pragma unroll
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(smem + off_ring + st * C::kRaw + hf * C::kHalf16 + j * 2048, tm, hf * 64, h, row0[j],
+                        &bar[st]);
+        }
+      }
+    };
+    // the slot of stage t is free (t >= R): its previous stage is consumed
+    auto slot_free = [&](uint64_t* bar, int t) -> bool {
+      const bool ok = t < R || wait_or_abort(&bar[t % R], ((t / R) - 1) & 1, abort);
+      return __all_sync(kFull, ok);
+    };
+    int kiss = 0, viss = 0;
+    bool ok = true;
+    int rk[C::kStageBlocks], rvw[C::kStageBlocks];
+    stage_rows(0, rk);
+    if (lane == 0) load(&tm_k, C::kOffRawK, kfull, rk, 0);
+    kiss = 1;
+    for (int t = 0; t < nstage; ++t) {
+#pragma unroll
+      for (int j = 0; j < C::kStageBlocks; ++j) rvw[j] = rk[j];  // rows of stage t, for V
+      if (t + 1 < nstage) {
+        stage_rows(t + 1, rk);
+        if (!slot_free(kfree, t + 1)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) load(&tm_k, C::kOffRawK, kfull, rk, t + 1);
+        kiss = t + 2;
+      }
+      if (!slot_free(vfree, t)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) load(&tm_v, C::kOffRawV, vfull, rvw, t);
+      viss = t + 1;
     }
     if (lane == 0) {
       if (!ok && !*abort) fail();
       // nothing may be in flight when the CTA exits: the last stages issued have landed
-      for (int t = max(0, issued - R); t < issued; ++t)
-        if (!mbar_wait(&full[t % R], (t / R) & 1)) break;
+      for (int t = max(0, kiss - R); t < kiss; ++t)
+        if (!mbar_wait(&kfull[t % R], (t / R) & 1)) break;
+      for (int t = max(0, viss - R); t < viss; ++t)
+        if (!mbar_wait(&vfull[t % R], (t / R) & 1)) break;
     }
     __syncwarp();
   } else if (!soft) {
@@ -406,38 +432,42 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
     if constexpr (FP8) {
       const int ct = threadIdx.x - C::kConvWarp0 * 32;  // 0 .. 127
       constexpr int kChunks = C::kKeys * (D / 8);  // 8-code chunks per tile
-      for (int t = 0; t < nstage; ++t) {
-        const int rs = t % R, es = t % E;
-        bool ok = wait_or_abort(&full[rs], (t / R) & 1, abort);
-        if (ok && t >= E) ok = wait_or_abort(&exp_empty[es], ((t / E) - 1) & 1, abort);
+      // expand one raw tile of stage t into its 16-bit slot, in the producer's order (K of
+      // stage t + 1 before V of stage t): K once S of the slot's previous stage is done, V once
+      // O += P V of it is done; false once the CTA aborts
+      auto expand = [&](int t, bool isv) -> bool {
+        bool ok = wait_or_abort(isv ? &vfull[t % R] : &kfull[t % R], (t / R) & 1, abort);
+        if (ok && t >= E) ok = wait_or_abort(isv ? &evfree[t % E] : &ekfree[t % E], ((t / E) - 1) & 1, abort);
         if (!ok && !*abort) fail();
         if (ok) {
-          const uint8_t* rk = smem + C::kOffRawK + rs * C::kRaw;
-          const uint8_t* rvv = smem + C::kOffRawV + rs * C::kRaw;
-          const uint32_t ek = smem_u32(smem + C::kOffExpK + es * C::kTile16);
-          const uint32_t ev = smem_u32(smem + C::kOffExpV + es * C::kTile16);
+          const uint8_t* raw = smem + (isv ? C::kOffRawV : C::kOffRawK) + (t % R) * C::kRaw;
+          const uint32_t dst0 = smem_u32(smem + (isv ? C::kOffExpV : C::kOffExpK) + (t % E) * C::kTile16);
 #pragma unroll 4
-          for (int i = 0; i < 2 * kChunks / 128; ++i) {
-            const int ci = ct + 128 * i;
-            const bool isv = ci >= kChunks;
-            const int cj = isv ? ci - kChunks : ci;
+          for (int i = 0; i < kChunks / 128; ++i) {
+            const int cj = ct + 128 * i;
             const int kr = cj / (D / 8), c = cj % (D / 8);
-            const uint2 raw = *reinterpret_cast<const uint2*>((isv ? rvv : rk) + kr * D + c * 8);
+            const uint2 w = *reinterpret_cast<const uint2*>(raw + kr * D + c * 8);
             const uint32_t dst =
-                (isv ? ev : ek) + (c >> 3) * C::kHalf16 + (kr >> 3) * 1024 + (kr & 7) * 128 + (((c & 7) ^ (kr & 7)) << 4);
-            st_shared_v4(dst, e4m3x2_to_f16x2(static_cast<uint16_t>(raw.x & 0xffffu)),
-                         e4m3x2_to_f16x2(static_cast<uint16_t>(raw.x >> 16)),
-                         e4m3x2_to_f16x2(static_cast<uint16_t>(raw.y & 0xffffu)),
-                         e4m3x2_to_f16x2(static_cast<uint16_t>(raw.y >> 16)));
+                dst0 + (c >> 3) * C::kHalf16 + (kr >> 3) * 1024 + (kr & 7) * 128 + (((c & 7) ^ (kr & 7)) << 4);
+            st_shared_v4(dst, e4m3x2_to_f16x2(static_cast<uint16_t>(w.x & 0xffffu)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(w.y & 0xffffu)),
+                         e4m3x2_to_f16x2(static_cast<uint16_t>(w.y >> 16)));
           }
         }
-        fence_proxy_async_smem();  // the expanded tiles are read by the tensor cores
+        fence_proxy_async_smem();  // the expanded tile is read by the tensor cores
         // every converter thread reaches this, failed or not, and all leave together
-        if (named_sync_or(1, 128, *abort != 0)) break;
+        if (named_sync_or(1, 128, *abort != 0)) return false;
         if (ct == 0) {
-          mbar_arrive(&raw_empty[rs]);  // the raw slot is read
-          mbar_arrive(&exp_full[es]);   // the expanded stage is complete
+          mbar_arrive(isv ? &vfree[t % R] : &kfree[t % R]);    // the raw slot is read
+          mbar_arrive(isv ? &evfull[t % E] : &ekfull[t % E]);  // the expanded tile is complete
         }
+        return true;
+      };
+      bool ok = expand(0, false);
+      for (int t = 0; t < nstage && ok; ++t) {
+        if (t + 1 < nstage) ok = expand(t + 1, false);
+        if (ok) ok = expand(t, true);
       }
     }
   } else {
@@ -453,8 +483,9 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
         break;
       }
       tc_fence_after();
+      const uint32_t scol = tmem + lane_base + C::kColS + 64 * b;
       float sv[64];
-      tmem_ld64(tmem + lane_base + C::kColS + 64 * b, sv);
+      tmem_ld64(scol, sv);
       const int nkeys = min(C::kKeys, (blk1 - blk0 - t * C::kStageBlocks) * kBlockSize);
       // keys past the split (the last stage only) take no part in the extreme below and get
       // weight 0; the row max of the scaled scores is the scale times the max (scale >= 0)
@@ -482,20 +513,17 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
         m_used = mx;
       }
       const float negm = -m_used;
-      // P row r: 64 weights 2^(s * scale - m) <= 2^8 as 16-bit values, 128-byte swizzled
-      // K-major (8 chunks of 8 keys).  bf16 pools: hi + lo parts (about 16 bits together)
-      // and l sums the fp32 weights; E4M3 pools: fp16 weights and l sums the rounded ones,
+      // P row r: 64 weights 2^(s * scale - m) <= 2^8 as 16-bit pairs over the S columns just
+      // read, 16 keys (8 columns) at a time.  bf16 pools: hi at +0, lo at +32 (about 16 bits
+      // together), l sums the fp32 weights; E4M3 pools: fp16 weights, l sums the rounded ones,
       // so O / l weighs V by the weights the MMAs use
-      const uint32_t roff = (r >> 3) * 1024 + (r & 7) * 128;
-      const uint32_t prow = p_tile(t) + roff;
-      const uint32_t plrow = C::kPSplit ? plo_tile(t) + roff : 0u;
       float ls = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4], wl[4];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[8], wl[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = 8 * c + 2 * e;
+        for (int e = 0; e < 8; ++e) {
+          const int k = 16 * c + 2 * e;
           float a = fast_exp2(fmaf(sv[k], sscale, negm));
           float bb = fast_exp2(fmaf(sv[k + 1], sscale, negm));
           if (partial) {  // a zero scale makes the masked products NaN: weight 0 by selection
@@ -508,12 +536,14 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
             ls += a + bb;
           } else {
             w[e] = pack_f16(a, bb);
+            wl[e] = 0u;
             ls += sum16<true>(w[e]);
           }
         }
-        st_shared_v4(prow + ((c ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
-        if constexpr (C::kPSplit) st_shared_v4(plrow + ((c ^ (r & 7)) << 4), wl[0], wl[1], wl[2], wl[3]);
+        tmem_st8(scol + 8 * c, w);
+        if constexpr (C::kPSplit) tmem_st8(scol + 32 + 8 * c, wl);
       }
+      tmem_wait_st();
       l += ls;
       // O += P V of stage t - 1 is done.  Waited at every stage, rescale or not: a parity
       // wait is unambiguous only while the barrier is at most one phase past the waiter,
@@ -537,7 +567,6 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
           tmem_st32(tmem + lane_base + C::kColO + 32 * ch, o);
         }
       }
-      fence_proxy_async_smem();  // P is read by the tensor cores
       tc_fence_before();
       __syncwarp();  // the warp's P rows and O rescales are done
       if (lane == 0) mbar_arrive(&p_full[b]);
@@ -571,24 +600,68 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, 1)
   }
 }
 
+namespace {
+
+// Shared-memory size set once per device and kernel, and the CTAs an SM holds, counted from
+// the SM's resources: shared memory (each CTA also takes the per-block reserve), registers
+// (allocated per warp in units of 256) and warps; then checked against the SM's 512
+// tensor-memory columns (an allocation that cannot be met would wait for a CTA that cannot
+// finish first).  The runtime's occupancy query was seen to report one CTA where the
+// profiler's limits and the runs show two.  0 on failure, with the error in *err.
+template <int D, bool FP8>
+int prefix_tc_configure(int device, cudaError_t* err) {
+  using C = TcPrefixCfg<D, FP8>;
+  static int per_sm_of[64] = {};
+  *err = cudaSuccess;
+  if (device < 0 || device >= 64) {
+    *err = cudaErrorInvalidDevice;
+    return 0;
+  }
+  if (per_sm_of[device] > 0) return per_sm_of[device];
+  auto kern = cascade_prefix_tc_kernel<D, FP8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
+  // the largest shared-memory carveout, so that every CTA the shared memory can hold fits
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  cudaFuncAttributes fa{};
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+  int smem_sm = 0, reserve = 0, regs_sm = 0, threads_sm = 0;
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserve, cudaDevAttrReservedSharedMemoryPerBlock, device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, device);
+  if (e != cudaSuccess) {
+    *err = e;
+    return 0;
+  }
+  const long long smem_cta = static_cast<long long>(C::kBytes) + fa.sharedSizeBytes + reserve;
+  const long long regs_warp = (static_cast<long long>(fa.numRegs) * 32 + 255) / 256 * 256;
+  const int warps = C::kThreads / 32;
+  long long per_sm = smem_sm / smem_cta;
+  per_sm = std::min(per_sm, regs_sm / (regs_warp * warps));
+  per_sm = std::min(per_sm, static_cast<long long>(threads_sm / 32 / warps));
+  if (per_sm < 1 || per_sm * C::kTmemCols > 512) {
+    *err = cudaErrorInvalidConfiguration;
+    return 0;
+  }
+  per_sm_of[device] = static_cast<int>(per_sm);
+  return per_sm_of[device];
+}
+
+}  // namespace
+
+template <int D, bool FP8>
+int cascade_prefix_tc_ctas_per_sm(int device) {
+  cudaError_t e;
+  return prefix_tc_configure<D, FP8>(device, &e);
+}
+
 template <int D, bool FP8>
 cudaError_t launch_cascade_prefix_tc(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p, dim3 grid,
                                      cudaStream_t stream, int device) {
   using C = TcPrefixCfg<D, FP8>;
-  auto kern = cascade_prefix_tc_kernel<D, FP8>;
-  static bool configured[64] = {};
-  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-  if (!configured[device]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
-    if (e != cudaSuccess) return e;
-    // tensor memory: the CTAs that can share an SM must not ask for more than its 512
-    // columns, or an allocation would wait for a CTA that cannot finish first
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, C::kBytes);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1 || per_sm * C::kTmemCols > 512) return cudaErrorInvalidConfiguration;
-    configured[device] = true;
-  }
+  cudaError_t e;
+  if (prefix_tc_configure<D, FP8>(device, &e) == 0) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -599,10 +672,11 @@ cudaError_t launch_cascade_prefix_tc(const CUtensorMap& tk, const CUtensorMap& t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, cascade_prefix_tc_kernel<D, FP8>, tk, tv, p);
 }
 
 #define PKV_DEFINE_PREFIX_TC(D, FP8)                                                                              \
+  template int cascade_prefix_tc_ctas_per_sm<D, FP8>(int);                                                       \
   template cudaError_t launch_cascade_prefix_tc<D, FP8>(const CUtensorMap&, const CUtensorMap&, const PrefixParams&, \
                                                         dim3, cudaStream_t, int);
 PKV_DEFINE_PREFIX_TC(64, false)

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -204,23 +205,22 @@ bool encode_kv_map_sw128(CUtensorMap* tm, void* base, int64_t num_blocks, int hk
 
 // Splits of the prefix pass: each split is a run of whole 64-key stages (a multiple of four
 // blocks), at least two stages long, at most kMaxPrefixRecords per prefix; the count
-// minimises (waves of CTAs, one resident per SM) x (blocks per split + 8), the 8 blocks
-// standing for a CTA's start-up and the merge work every extra record adds; the fewest
-// splits on a tie.  PKV_PREFIX_SPLIT_BLOCKS (>= 4) fixes the blocks per split, for tuning
-// and tests.
+// minimises (waves of CTAs, `slots` = SMs x CTAs resident per SM at a time) x (blocks per
+// split + 8), the 8 blocks standing for a CTA's start-up and the merge work every extra
+// record adds; the fewest splits on a tie.  PKV_PREFIX_SPLIT_BLOCKS (>= 4) fixes the blocks
+// per split, for tuning and tests.
 struct PrefixPlan {
-  int tiles;         // 64-row query tiles per prefix
+  int tiles;         // 128-row query tiles per prefix
   int pre_slots;     // splits per prefix
   int split_blocks;  // prefix blocks per split
 };
 
-PrefixPlan plan_prefix(int num_prefixes, int max_members, int max_prefix_len, int g, int hkv, int sm_count) {
+PrefixPlan plan_prefix(int num_prefixes, int max_members, int max_prefix_len, int g, int hkv, long long slots) {
   PrefixPlan pp{0, 0, 0};
   const int pblocks = (max_prefix_len + 15) / 16;
   if (num_prefixes <= 0 || max_members <= 0 || pblocks <= 0) return pp;
   pp.tiles = static_cast<int>((static_cast<long long>(max_members) * g + 127) / 128);
   const long long per_split = static_cast<long long>(pp.tiles) * hkv * num_prefixes;
-  const long long slots = sm_count;  // one CTA per SM
   if (const char* env = std::getenv("PKV_PREFIX_SPLIT_BLOCKS")) {  // tuning and tests: blocks per split
     const long v = std::strtol(env, nullptr, 10);
     if (v >= 4) {
@@ -416,8 +416,23 @@ size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
   }
   DeviceInfo* dev = nullptr;
   if (device_info(&dev) != PKV_OK) return 0;
-  const PrefixPlan pp = plan_prefix(num_prefixes, max_members, max_prefix_len, num_q_heads / num_kv_heads,
-                                    num_kv_heads, dev->sm_count);
+  // the most prefix records either pool type plans for (its CTAs per SM set the splits)
+  int device = 0;
+  cudaGetDevice(&device);
+  const int per_sm[2] = {head_dim == 64 ? pkv::cascade_prefix_tc_ctas_per_sm<64, false>(device)
+                                        : pkv::cascade_prefix_tc_ctas_per_sm<128, false>(device),
+                         head_dim == 64 ? pkv::cascade_prefix_tc_ctas_per_sm<64, true>(device)
+                                        : pkv::cascade_prefix_tc_ctas_per_sm<128, true>(device)};
+  PrefixPlan pp{0, 0, 0};
+  for (int k = 0; k < 2; ++k) {
+    if (per_sm[k] <= 0) {
+      fail(PKV_ERR_CUDA, "the prefix pass does not fit on an SM of this device");
+      return 0;
+    }
+    const PrefixPlan pk = plan_prefix(num_prefixes, max_members, max_prefix_len, num_q_heads / num_kv_heads,
+                                      num_kv_heads, static_cast<long long>(dev->sm_count) * per_sm[k]);
+    if (pk.pre_slots > pp.pre_slots) pp = pk;
+  }
   Split sp;
   WsLayout ws;
   Variant var;
@@ -577,7 +592,17 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   const int g = num_q_heads / hkv;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != PKV_OK) return st;
-  const PrefixPlan pp = plan_prefix(px->num_prefixes, px->max_members, px->max_prefix_len, g, hkv, dev->sm_count);
+  const bool fp8 = cache->kv_dtype == PKV_KV_FP8_E4M3;
+  int device = 0;
+  cudaGetDevice(&device);
+  const int per_sm = cache->head_dim == 64
+                         ? (fp8 ? pkv::cascade_prefix_tc_ctas_per_sm<64, true>(device)
+                                : pkv::cascade_prefix_tc_ctas_per_sm<64, false>(device))
+                         : (fp8 ? pkv::cascade_prefix_tc_ctas_per_sm<128, true>(device)
+                                : pkv::cascade_prefix_tc_ctas_per_sm<128, false>(device));
+  if (per_sm <= 0) return fail(PKV_ERR_CUDA, "the prefix pass does not fit on an SM of this device");
+  const PrefixPlan pp = plan_prefix(px->num_prefixes, px->max_members, px->max_prefix_len, g, hkv,
+                                    static_cast<long long>(dev->sm_count) * per_sm);
   if (static_cast<long long>(px->num_prefixes) * pp.pre_slots > 65535 || pp.tiles > 0x7fffffff / 2)
     return fail(PKV_ERR_UNSUPPORTED, "too many prefixes for the prefix-pass grid");
   Split sp;
@@ -593,7 +618,6 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   if (!q || !aligned(q, 16)) return fail(PKV_ERR_INVALID_ARG, "q must be non-NULL and 16-byte aligned");
   if (!std::isfinite(softmax_scale)) return fail(PKV_ERR_INVALID_ARG, "softmax_scale must be finite");
 
-  const bool fp8 = cache->kv_dtype == PKV_KV_FP8_E4M3;
   CUtensorMap tk, tv;
   const bool maps_ok =
       fp8 ? encode_kv_map(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim, true) &&
@@ -623,8 +647,6 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   pr.rec_slots = pp.pre_slots + sp.max_splits;
   pr.score_scale = softmax_scale * 1.4426950408889634f;  // log2(e)
   pr.scales = cache->scales;
-  int device = 0;
-  cudaGetDevice(&device);
   const dim3 pgrid(static_cast<unsigned>(pp.tiles), static_cast<unsigned>(hkv),
                    static_cast<unsigned>(px->num_prefixes * pp.pre_slots));
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
