@@ -61,6 +61,7 @@ struct DecodeParams {
   int rec_slots;        // records per (b, h): pre_slots + max_splits
   float score_scale;    // softmax_scale * log2(e)
   int out_fp32;
+  int merge_warps;      // merge kernel: warps per query head (1, 2, 4 or 8; set by its launch)
 };
 
 template <int D, int G, bool FP8, int NWC, int STAGES>
