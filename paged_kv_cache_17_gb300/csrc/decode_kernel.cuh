@@ -62,6 +62,8 @@ struct DecodeParams {
   float score_scale;    // softmax_scale * log2(e)
   int out_fp32;
   int merge_warps;      // merge kernel: warps per query head (1, 2, 4 or 8; set by its launch)
+  int defer_prefix;     // cascade: the decode writes a record for every prefixed sequence and
+                        // the merge kernel combines it with the prefix records (tensor-core form)
 };
 
 template <int D, int G, bool FP8, int NWC, int STAGES>

@@ -96,11 +96,23 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   const int hq0 = h * G;
   int npre = 0;
   if constexpr (CAS) npre = p.seq_prefix[b] >= 0 ? p.pre_slots : 0;
+  // Deferred cascade merge: a prefixed sequence's result goes out as a record, which the
+  // merge kernel combines with the prefix records, so no CTA waits here for the prefix pass
+  // but one, which keeps this grid from completing before the prefix grid (the merge kernel
+  // waits for this grid).  Otherwise every cascade CTA waits before it exits.
+  const bool defer = CAS && p.defer_prefix != 0;
+  auto end_wait = [&]() {
+    if constexpr (CAS) {
+      if (!defer || (blockIdx.x | blockIdx.y | blockIdx.z) == 0) pdl_wait();
+    }
+  };
   if (nblk == 0) {  // no own blocks: partition 0 writes zeros, or the prefix result alone
     if (s == 0) {
       if (CAS && npre > 0) {
-        pdl_wait();
-        merge_records<D, G, FP8>(p, b, h, 0, npre, reinterpret_cast<float*>(smem), C::kThreads);
+        if (!defer) {  // deferred: the merge kernel takes the prefix records alone
+          pdl_wait();
+          merge_records<D, G, FP8>(p, b, h, 0, npre, reinterpret_cast<float*>(smem), C::kThreads);
+        }
       } else {
         for (int e = threadIdx.x; e < G * D; e += C::kThreads) {
           const size_t o = (static_cast<size_t>(b) * p.hq + hq0) * D + e;
@@ -109,11 +121,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         }
       }
     }
-    if constexpr (CAS) pdl_wait();
+    end_wait();
     return;
   }
   if (s >= nsplit) {
-    if constexpr (CAS) pdl_wait();
+    end_wait();
     return;
   }
   const int nloc = min(nblk, blk0 + p.split_blocks) - blk0;
@@ -353,7 +365,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
 
   const size_t out_row0 = static_cast<size_t>(b) * p.hq + hq0;
   const bool single = (nsplit == 1 && npre == 0);
-  const bool with_prefix = CAS && (nsplit == 1 && npre > 0);
+  const bool with_prefix = CAS && !defer && (nsplit == 1 && npre > 0);
   const size_t prec0 = (static_cast<size_t>(b) * p.hkv + h) * p.rec_slots;
   if (CAS && with_prefix) {
     // One partition plus the shared-prefix records: per head the total max over the warps
@@ -457,7 +469,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   // A record was written (or, for one partition, the output): the merge kernel that
   // follows combines the records.  A cascade grid completes only after the prefix pass,
   // whose records the merge kernel also reads.
-  if constexpr (CAS) pdl_wait();
+  end_wait();
 }
 
 }  // namespace pkv

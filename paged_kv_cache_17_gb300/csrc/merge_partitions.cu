@@ -35,8 +35,10 @@ __global__ void __launch_bounds__(256) merge_partitions_kernel(const DecodeParam
   len = len < 0 ? 0 : (len > cap ? cap : len);
   const int nblk = (len + kBlockSize - 1) / kBlockSize;
   const int nsplit = (nblk + p.split_blocks - 1) / p.split_blocks;
-  if (nsplit <= 1) return;  // one partition: the decode kernel wrote the output itself (CTA-uniform)
   const int npre = (p.seq_prefix != nullptr && p.seq_prefix[b] >= 0) ? p.pre_slots : 0;
+  // one partition and no deferred prefix records: the decode kernel wrote the output itself
+  // (CTA-uniform)
+  if (nsplit <= 1 && !(p.defer_prefix && npre > 0)) return;
   const int lo = p.pre_slots - npre, hi = p.pre_slots + nsplit;
   const int W = p.merge_warps;          // warps per query head
   const int gl = warp / W, wk = warp % W;

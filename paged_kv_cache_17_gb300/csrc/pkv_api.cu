@@ -527,13 +527,23 @@ pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32
   p.rec_slots = pre_slots + sp.max_splits;
   p.score_scale = softmax_scale * 1.4426950408889634f;  // log2(e)
   p.out_fp32 = out_dtype == PKV_OUT_FP32;
+  // Where the tensor-core decode merges the prefix records.  bf16 pools: in the merge kernel,
+  // so that no decode CTA waits for the prefix pass, which runs beside the decode (one
+  // prefix CTA per SM; see the cascade call).  E4M3 pools: in the decode CTA, after the
+  // prefix pass (an E4M3 decode CTA is larger and little would run beside it).
+  // PKV_CASCADE_DEFER (0 or 1) overrides this, for tuning and tests.
+  if (pre_slots > 0 && var.swizzled) {
+    bool defer = !fp8;
+    if (const char* env = std::getenv("PKV_CASCADE_DEFER")) defer = env[0] == '1';
+    p.defer_prefix = defer ? 1 : 0;
+  }
   int device = 0;
   cudaGetDevice(&device);
   const dim3 grid(static_cast<unsigned>(cache->num_kv_heads), static_cast<unsigned>(batch),
                   static_cast<unsigned>(sp.max_splits));
   cudaError_t e = var.launch(tk, tv, p, grid, reinterpret_cast<cudaStream_t>(stream), device);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (sp.max_splits > 1) {  // sequences split into several partitions: merge their records
+  if (sp.max_splits > 1 || p.defer_prefix) {  // records to merge: split sequences, deferred prefixes
     e = pkv::launch_merge_partitions(cache->head_dim, num_q_heads / cache->num_kv_heads, fp8, p,
                                      dim3(static_cast<unsigned>(cache->num_kv_heads), static_cast<unsigned>(batch)),
                                      reinterpret_cast<cudaStream_t>(stream));
@@ -601,8 +611,17 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
                          : (fp8 ? pkv::cascade_prefix_tc_ctas_per_sm<128, true>(device)
                                 : pkv::cascade_prefix_tc_ctas_per_sm<128, false>(device));
   if (per_sm <= 0) return fail(PKV_ERR_CUDA, "the prefix pass does not fit on an SM of this device");
+  // bf16 pools: one prefix CTA per SM, so that three decode CTAs share each SM with it and
+  // stream the sequences' own blocks while the prefix pass runs (shared-prefix step 82.7 ->
+  // 75.4 us); E4M3 pools: every CTA an SM holds (the prefix pass is the longer part there,
+  // fork step 76.9 -> 64.8 us).  PKV_PREFIX_CTAS_PER_SM overrides this, for tuning and tests.
+  int plan_per_sm = fp8 ? per_sm : 1;
+  if (const char* env = std::getenv("PKV_PREFIX_CTAS_PER_SM")) {
+    const long v = std::strtol(env, nullptr, 10);
+    if (v >= 1 && v <= per_sm) plan_per_sm = static_cast<int>(v);
+  }
   const PrefixPlan pp = plan_prefix(px->num_prefixes, px->max_members, px->max_prefix_len, g, hkv,
-                                    static_cast<long long>(dev->sm_count) * per_sm);
+                                    static_cast<long long>(dev->sm_count) * plan_per_sm);
   if (static_cast<long long>(px->num_prefixes) * pp.pre_slots > 65535 || pp.tiles > 0x7fffffff / 2)
     return fail(PKV_ERR_UNSUPPORTED, "too many prefixes for the prefix-pass grid");
   Split sp;

@@ -52,12 +52,14 @@ def env(**kv):
                 os.environ[k] = v
 
 
-def build(hkv, g, d, members, pblocks, seed, grow=0.0):
-    """`members` sequences share a prefix of `pblocks` blocks and own 1..40 tokens each; with
-    grow > 0 the K rows of prefix block j are multiplied by (1 + grow * j) before rounding to
-    bf16, so later keys score higher and the running max climbs stage after stage."""
+def build(hkv, g, d, members, pblocks, seed, grow=0.0, no_own=0):
+    """`members` sequences share a prefix of `pblocks` blocks and own 1..40 tokens each (the
+    first `no_own` members none: the prefix is their whole context); with grow > 0 the K rows
+    of prefix block j are multiplied by (1 + grow * j) before rounding to bf16, so later keys
+    score higher and the running max climbs stage after stage."""
     gen = torch.Generator().manual_seed(seed)
     own = torch.randint(1, 41, (members,), generator=gen).tolist()
+    own = [0] * no_own + own[no_own:]
     nb = pblocks + sum(W.blocks_for_tokens(n) for n in own) + 8
     pool = W.BlockPool(nb, generator=gen)
     prefix = pool.allocate(pblocks)
@@ -146,3 +148,28 @@ def test_many_short_splits_are_capped(pkv):
     ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
                             lens.numpy(), scale)
     assert_close(got, ref, "bf16", "capped prefix splits")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("defer,per_sm", [("0", "1"), ("1", "1"), ("0", "2"), ("1", "2")])
+def test_merge_placement_and_prefix_occupancy(pkv, fp8, defer, per_sm):
+    """The prefix records merged in the decode CTA (0) or by the merge kernel after it (1),
+    with the prefix pass planned for one or two CTAs per SM: the same result, including
+    members without blocks of their own (the prefix alone)."""
+    c, kp, vp, q, full, lens = build(2, 4, 128, 45, 40, seed=900 + int(fp8), no_own=3)
+    scale = 128 ** -0.5
+    if fp8:
+        k8, ks = quant_e4m3(kp)
+        v8, vs = quant_e4m3(vp)
+        scales = torch.stack([ks, vs]).contiguous()
+        with env(PKV_CASCADE_DEFER=defer, PKV_PREFIX_CTAS_PER_SM=per_sm, PKV_PREFIX_SPLIT_BLOCKS=8):
+            got = run(pkv, c, k8.cuda(), v8.cuda(), q, scale, scales=scales)
+        ref = oracle.decode_all(W.bf16_bits(q), k8.numpy(), v8.numpy(), oracle.KV_E4M3, full.numpy(), lens.numpy(),
+                                scale, scales=scales.numpy())
+        assert_close(got, ref, "fp8", f"e4m3 defer={defer} per_sm={per_sm}")
+    else:
+        with env(PKV_CASCADE_DEFER=defer, PKV_PREFIX_CTAS_PER_SM=per_sm, PKV_PREFIX_SPLIT_BLOCKS=8):
+            got = run(pkv, c, kp.cuda(), vp.cuda(), q, scale)
+        ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
+                                lens.numpy(), scale)
+        assert_close(got, ref, "bf16", f"bf16 defer={defer} per_sm={per_sm}")
