@@ -171,7 +171,9 @@ int32_t pkv_decode_partition_tokens(int32_t batch, int32_t num_kv_heads, int32_t
  *   for E4M3 pools times a per-head power of two rounded to fp16 (relative error at most
  *   2^-11); the softmax weights enter as a 16-bit hi + lo pair.  While the environment
  *   variable PKV_DECODE_CUDA_CORES is "1" (read at each call), every product runs in fp32
- *   on the CUDA cores instead.
+ *   on the CUDA cores instead.  PKV_SPLIT_TOKENS (a positive multiple of 16, read at each
+ *   call and by pkv_decode_workspace_size) fixes the partition length (tuning; the
+ *   workspace size follows it).
  *   workspace: device memory of at least pkv_decode_workspace_size(...) bytes, 256-byte
  *   aligned, any contents; may be NULL when the required size is 0.
  */
@@ -231,6 +233,11 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const
  *   weights enter the P V product as a bf16 hi + lo pair (about 16 significant bits);
  *   E4M3 pools expand the codes exactly to fp16, multiply fp16 q (q rounded to fp16, exact
  *   for |q| in 2^-14 .. 65504) and fp16 weights, whose rounded sum is the denominator.
+ *   Tuning (environment, read at each call; results agree within the tolerances above):
+ *   PKV_PREFIX_SPLIT_BLOCKS (>= 4) fixes the prefix blocks per split of the prefix pass,
+ *   PKV_PREFIX_CTAS_PER_SM (1 or 2) the prefix-pass CTAs an SM is planned for, and
+ *   PKV_CASCADE_DEFER (0 or 1) whether the prefix records are merged in the decode kernel (0)
+ *   or by the merge kernel after it (1); PKV_SPLIT_TOKENS applies as for the plain decode.
  */
 typedef struct {
   const int32_t* prefix_tables;  /* [num_prefixes][max_prefix_blocks] physical block ids */
