@@ -4,6 +4,9 @@ log-sum-exp weights.  The reference is the oracle's plain decode over each seque
 whole table (prefix blocks, then its own): the split is exact (habr.com/ru/articles/1021832,
 section 3), so the two must agree within the bf16 tolerance -- the prefix pass rounds the
 softmax weights to bf16 for its tensor-core P V product."""
+import os
+from contextlib import contextmanager
+
 import numpy as np
 import pytest
 import torch
@@ -26,6 +29,21 @@ def pkv():
 
     m.check_device_status()
     return m
+
+
+@contextmanager
+def env(**kv):
+    old = {k: os.environ.get(k) for k in kv}
+    try:
+        for k, v in kv.items():
+            os.environ[k] = str(v)
+        yield
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
 
 
 def run_cascade(pkv, q, kd, vd, c: W.CascadeInputs, scale, out_dtype=torch.float32):
@@ -98,15 +116,32 @@ def test_edge_cases(pkv, hkv, g, d):
     assert_close(out.cpu().double().numpy(), ref, "bf16", f"cascade edges hkv={hkv} g={g} d={d}")
 
 
+@pytest.mark.parametrize("defer", ["0", "1"])
 @pytest.mark.parametrize("split", [16, 64])
-def test_split_suffixes_merge_with_prefix(pkv, split):
+def test_split_suffixes_merge_with_prefix(pkv, split, defer):
+    """Suffixes in several partitions, merged with the prefix records in the merge kernel
+    either way; defer=1 also sends single-partition suffixes there."""
     c, kp, vp, q, full, lens = build_case(2, 4, 128, seed=5)
-    with split_tokens(split):
+    with split_tokens(split), env(PKV_CASCADE_DEFER=defer):
         out = run_cascade(pkv, q.cuda(), kp.cuda(), vp.cuda(), c, 0.1, out_dtype=torch.bfloat16)
     assert pkv.check_device_status() == 0
     ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
                             lens.numpy(), 0.1)
-    assert_close(out.cpu().double().numpy(), ref, "bf16", f"cascade split {split}")
+    assert_close(out.cpu().double().numpy(), ref, "bf16", f"cascade split {split} defer {defer}")
+
+
+@pytest.mark.parametrize("hkv,g,d", [(2, 4, 128), (1, 8, 128), (4, 1, 64)])
+def test_cascade_on_cuda_core_decode(pkv, hkv, g, d):
+    """The cascade with the CUDA-core decode form (PKV_DECODE_CUDA_CORES=1) for the
+    sequences' own blocks: it merges the prefix records itself."""
+    c, kp, vp, q, full, lens = build_case(hkv, g, d, seed=31 + g + d)
+    scale = d ** -0.5
+    with env(PKV_DECODE_CUDA_CORES=1):
+        out = run_cascade(pkv, q.cuda(), kp.cuda(), vp.cuda(), c, scale)
+    assert pkv.check_device_status() == 0
+    ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
+                            lens.numpy(), scale)
+    assert_close(out.cpu().double().numpy(), ref, "bf16", f"cascade on CUDA cores hkv={hkv} g={g} d={d}")
 
 
 def test_no_prefixes_is_plain_decode(pkv):
