@@ -432,6 +432,7 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, TcPrefixCfg<D, 
     if constexpr (FP8) {
       const int ct = threadIdx.x - C::kConvWarp0 * 32;  // 0 .. 127
       constexpr int kChunks = C::kKeys * (D / 8);  // 8-code chunks per tile
+      static_assert((128 / (D / 8)) % 8 == 0, "a thread's rows keep their phase in the swizzle atom");
       // expand one raw tile of stage t into its 16-bit slot, in the producer's order (K of
       // stage t + 1 before V of stage t): K once S of the slot's previous stage is done, V once
       // O += P V of it is done; false once the CTA aborts
@@ -440,15 +441,17 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, TcPrefixCfg<D, 
         if (ok && t >= E) ok = wait_or_abort(isv ? &evfree[t % E] : &ekfree[t % E], ((t / E) - 1) & 1, abort);
         if (!ok && !*abort) fail();
         if (ok) {
-          const uint8_t* raw = smem + (isv ? C::kOffRawV : C::kOffRawK) + (t % R) * C::kRaw;
-          const uint32_t dst0 = smem_u32(smem + (isv ? C::kOffExpV : C::kOffExpK) + (t % E) * C::kTile16);
+          // thread ct takes the 8-code chunk c of rows k0, k0 + kRowsStep, ...: the row's phase in
+          // its 8-row swizzle atom never changes, so both addresses advance by constants
+          constexpr int kRowsStep = 128 / (D / 8);  // rows per pass of the 128 threads (8 or 16)
+          const int c = ct % (D / 8), k0 = ct / (D / 8);
+          const uint8_t* src = smem + (isv ? C::kOffRawV : C::kOffRawK) + (t % R) * C::kRaw + k0 * D + c * 8;
+          const uint32_t dst0 = smem_u32(smem + (isv ? C::kOffExpV : C::kOffExpK) + (t % E) * C::kTile16) +
+                                (c >> 3) * C::kHalf16 + (k0 >> 3) * 1024 + (k0 & 7) * 128 + (((c & 7) ^ (k0 & 7)) << 4);
 #pragma unroll 4
           for (int i = 0; i < kChunks / 128; ++i) {
-            const int cj = ct + 128 * i;
-            const int kr = cj / (D / 8), c = cj % (D / 8);
-            const uint2 w = *reinterpret_cast<const uint2*>(raw + kr * D + c * 8);
-            const uint32_t dst =
-                dst0 + (c >> 3) * C::kHalf16 + (kr >> 3) * 1024 + (kr & 7) * 128 + (((c & 7) ^ (kr & 7)) << 4);
+            const uint2 w = *reinterpret_cast<const uint2*>(src + i * kRowsStep * D);
+            const uint32_t dst = dst0 + i * (kRowsStep / 8) * 1024;
             st_shared_v4(dst, e4m3x2_to_f16x2(static_cast<uint16_t>(w.x & 0xffffu)),
                          e4m3x2_to_f16x2(static_cast<uint16_t>(w.x >> 16)),
                          e4m3x2_to_f16x2(static_cast<uint16_t>(w.y & 0xffffu)),
