@@ -37,7 +37,9 @@
 //
 // Each CTA is one chain of dependent steps (S -> weights -> O += P V) whose latency, not
 // any one unit's throughput, sets its pace; so two CTAs fit on an SM (shared memory at most
-// 98 KiB and 256 TMEM columns each) and their chains interleave.
+// 98 KiB and 256 TMEM columns each) and their chains interleave.  The host plans E4M3
+// passes for two CTAs per SM; bf16 passes for one, so that three decode CTAs share each SM
+// with it and stream the sequences' own blocks meanwhile.
 // Shared memory: Q (128 x D, 16-bit, 128-byte swizzled, K-major) and K and V rings ([column
 // half][64 keys][128 bytes], swizzled by the TMA load; 2 stages each at D = 128, 4 at
 // D = 64); E4M3 pools add rings of expanded fp16 tiles (1 stage each at D = 128, 2 at
