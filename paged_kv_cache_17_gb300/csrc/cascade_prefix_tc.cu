@@ -94,6 +94,13 @@ struct TcPrefixCfg {
 
 namespace {
 
+// 2^x by the hardware approximation with subnormal inputs and results flushed to zero
+__device__ __forceinline__ float exp2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // wait for a phase, giving up when the CTA has aborted or after the wait limit
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -518,6 +525,10 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, TcPrefixCfg<D, 
         m_used = mx;
       }
       const float negm = -m_used;
+      // 2^x of a weight.  E4M3 pools: the flush-to-zero form, fewer instructions (fork step
+      // 58.5 -> 56.7 us); exact in effect, as the fp16 weights turn everything below 2^-24
+      // into zero anyway.  bf16 pools keep the weights below 2^-126 (no gain measured there).
+      auto weight = [](float x) { return FP8 ? exp2_ftz(x) : fast_exp2(x); };
       // P row r: 64 weights 2^(s * scale - m) <= 2^8 as 16-bit pairs over the S columns just
       // read, 16 keys (8 columns) at a time.  bf16 pools: hi at +0, lo at +32 (about 16 bits
       // together), l sums the fp32 weights; E4M3 pools: fp16 weights, l sums the rounded ones,
@@ -529,8 +540,8 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, TcPrefixCfg<D, 
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int k = 16 * c + 2 * e;
-          float a = fast_exp2(fmaf(sv[k], sscale, negm));
-          float bb = fast_exp2(fmaf(sv[k + 1], sscale, negm));
+          float a = weight(fmaf(sv[k], sscale, negm));
+          float bb = weight(fmaf(sv[k + 1], sscale, negm));
           if (partial) {  // a zero scale makes the masked products NaN: weight 0 by selection
             a = k < nkeys ? a : 0.f;
             bb = k + 1 < nkeys ? bb : 0.f;
