@@ -256,7 +256,8 @@ using InfoFn = pkv::DecodeLaunchInfo (*)();
 struct Variant {
   LaunchFn launch;
   InfoFn info;
-  bool swizzled = false;  // the tensor-core form reads 128-byte-swizzled 64-column boxes
+  bool swizzled = false;     // the tensor-core form reads 128-byte-swizzled 64-column boxes (bf16)
+  bool tensor_core = false;  // the tensor-core form (either pool type)
 };
 
 template <int D, bool FP8, bool CAS>
@@ -273,11 +274,11 @@ Variant pick_g(int g) {
 template <int D, bool FP8, bool CAS>
 Variant pick_mma(int g) {
   switch (g) {
-    case 1: return {pkv::launch_decode_mma<D, 1, FP8, CAS>, pkv::decode_mma_launch_info<D, 1, FP8, CAS>, !FP8};
-    case 2: return {pkv::launch_decode_mma<D, 2, FP8, CAS>, pkv::decode_mma_launch_info<D, 2, FP8, CAS>, !FP8};
-    case 4: return {pkv::launch_decode_mma<D, 4, FP8, CAS>, pkv::decode_mma_launch_info<D, 4, FP8, CAS>, !FP8};
-    case 8: return {pkv::launch_decode_mma<D, 8, FP8, CAS>, pkv::decode_mma_launch_info<D, 8, FP8, CAS>, !FP8};
-    default: return {nullptr, nullptr, false};
+    case 1: return {pkv::launch_decode_mma<D, 1, FP8, CAS>, pkv::decode_mma_launch_info<D, 1, FP8, CAS>, !FP8, true};
+    case 2: return {pkv::launch_decode_mma<D, 2, FP8, CAS>, pkv::decode_mma_launch_info<D, 2, FP8, CAS>, !FP8, true};
+    case 4: return {pkv::launch_decode_mma<D, 4, FP8, CAS>, pkv::decode_mma_launch_info<D, 4, FP8, CAS>, !FP8, true};
+    case 8: return {pkv::launch_decode_mma<D, 8, FP8, CAS>, pkv::decode_mma_launch_info<D, 8, FP8, CAS>, !FP8, true};
+    default: return {nullptr, nullptr, false, false};
   }
 }
 
@@ -532,7 +533,7 @@ pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32
   // prefix CTA per SM; see the cascade call).  E4M3 pools: in the decode CTA, after the
   // prefix pass (an E4M3 decode CTA is larger and little would run beside it).
   // PKV_CASCADE_DEFER (0 or 1) overrides this, for tuning and tests.
-  if (pre_slots > 0 && var.swizzled) {
+  if (pre_slots > 0 && var.tensor_core) {
     bool defer = !fp8;
     if (const char* env = std::getenv("PKV_CASCADE_DEFER")) defer = env[0] == '1';
     p.defer_prefix = defer ? 1 : 0;
