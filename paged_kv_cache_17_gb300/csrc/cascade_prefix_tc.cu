@@ -8,8 +8,9 @@
 // attention over one part of the keys is a running max m, a running sum l and an
 // unnormalised output, and parts combine with the rescale exp(m_part - m_total).  So the
 // prefix part of every member's decode attention is computed here once per prefix group;
-// each sequence's own blocks are handled by the decode kernel, which merges these partial
-// results as extra partitions.  Per (kv head, prefix) the contraction is [member rows x
+// each sequence's own blocks are handled by the decode kernel, and these partial results
+// join its own as extra partitions (merged by the merge kernel after the decode, or in the
+// decode CTA).  Per (kv head, prefix) the contraction is [member rows x
 // prefix keys], dense and large enough for the 128-row MMAs:
 //
 //   S [128 rows x 64 keys] = Q [128 x D] K^T          (tcgen05.mma kind::f16, fp32 in TMEM)
