@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(TcPrefixCfg<D, FP8>::kThreads, TcPrefixCfg<D, 
     // ======================================================================== TMA producer
     // block ids of the split, 32 (eight stages) at a time in the lanes, the next 32 in flight;
     // K of stage t + 1 goes before V of stage t (its slot frees earlier: when S of stage
-    // t - 1 is done, before O += P V of stage t - 2)
+    // t + 1 - R is done, before O += P V of stage t - R)
     const int nblk = blk1 - blk0;
     int ids = lane < nblk ? table[blk0 + lane] : 0;
     int nxt = 32 + lane < nblk ? table[blk0 + 32 + lane] : 0;
