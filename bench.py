@@ -104,7 +104,7 @@ def step_bytes(w: W.Workload) -> dict:
 
 def decode_kernel_name(cfg, cascade: bool) -> str:
     """The kernels inside the decode call's timed interval (the merge runs for split
-    sequences, and for bf16 cascades, whose prefix records it merges)."""
+    sequences, and for cascades, whose prefix records it merges)."""
     tc = os.environ.get("PKV_DECODE_CUDA_CORES") != "1"  # both pool types run the tensor-core form
     core = "paged_decode_mma_kernel (tensor cores)" if tc else "paged_decode_kernel (CUDA cores)"
     name = core + " + merge_partitions_kernel"
@@ -386,12 +386,11 @@ def run_ours(args):
     peak = peak or FALLBACK_HBM_GBS
 
     # our kernels per step: append, [prefix pass], decode, [merge: of split sequences, or of
-    # the prefix records, which the tensor-core decode leaves to it for bf16 pools]
+    # the prefix records, which the tensor-core decode leaves to it]
     dec_len = suffix_max if cas is not None else max_len
     has_prefix = cas is not None and cas.prefix_tables.shape[0] > 0
     tensor_core = os.environ.get("PKV_DECODE_CUDA_CORES") != "1"
-    deferred = has_prefix and tensor_core and os.environ.get(
-        "PKV_CASCADE_DEFER", "1" if cfg.kv_dtype == "bf16" else "0") == "1"
+    deferred = has_prefix and tensor_core and os.environ.get("PKV_CASCADE_DEFER", "1") == "1"
     split = dec_len > pkv.partition_tokens(B, hkv, dec_len)
     launches_per_step = 2 + (1 if has_prefix else 0) + (1 if split or deferred else 0)
 

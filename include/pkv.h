@@ -221,8 +221,8 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const
  * as a dense [members x G rows] x [prefix keys] contraction on the fifth-generation tensor
  * cores (tcgen05 MMAs of 128 query rows, fp32 accumulation in tensor memory); the
  * sequences' own blocks go through the decode kernel, and the prefix results are merged
- * with log-sum-exp weights (for bf16 pools by a merge kernel after the decode, so that the
- * prefix pass runs beside it; for E4M3 pools in the decode kernel).
+ * with log-sum-exp weights by a merge kernel after the decode (so that no decode CTA waits
+ * for the prefix pass; for bf16 pools the pass runs beside the decode).
  *   prefixes: see pkv_prefix_desc; may describe zero prefixes (then this is a plain decode).
  *   block_tables / context_lens: each sequence's blocks AFTER its prefix and their token
  *     count (its full table and length when it has no prefix); 0 is allowed when the

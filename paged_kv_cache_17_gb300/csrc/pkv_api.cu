@@ -528,13 +528,13 @@ pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32
   p.rec_slots = pre_slots + sp.max_splits;
   p.score_scale = softmax_scale * 1.4426950408889634f;  // log2(e)
   p.out_fp32 = out_dtype == PKV_OUT_FP32;
-  // Where the tensor-core decode merges the prefix records.  bf16 pools: in the merge kernel,
-  // so that no decode CTA waits for the prefix pass, which runs beside the decode (one
-  // prefix CTA per SM; see the cascade call).  E4M3 pools: in the decode CTA, after the
-  // prefix pass (an E4M3 decode CTA is larger and little would run beside it).
-  // PKV_CASCADE_DEFER (0 or 1) overrides this, for tuning and tests.
+  // Where the tensor-core decode merges the prefix records: in the merge kernel after it, so
+  // that no decode CTA waits for the prefix pass (for bf16 pools the pass runs beside the
+  // decode, one prefix CTA per SM; see the cascade call).  E4M3 fork step 56.3 us against
+  // 56.7 us with the merge in the decode CTA.  PKV_CASCADE_DEFER=0 merges in the decode CTA
+  // (tuning and tests).
   if (pre_slots > 0 && var.tensor_core) {
-    bool defer = !fp8;
+    bool defer = true;
     if (const char* env = std::getenv("PKV_CASCADE_DEFER")) defer = env[0] == '1';
     p.defer_prefix = defer ? 1 : 0;
   }
@@ -615,7 +615,7 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   // bf16 pools: one prefix CTA per SM, so that three decode CTAs share each SM with it and
   // stream the sequences' own blocks while the prefix pass runs (shared-prefix step 82.7 ->
   // 75.4 us); E4M3 pools: every CTA an SM holds (the prefix pass is the longer part there,
-  // fork step 76.9 -> 64.8 us).  PKV_PREFIX_CTAS_PER_SM overrides this, for tuning and tests.
+  // fork step 64.4 -> 56.3 us).  PKV_PREFIX_CTAS_PER_SM overrides this, for tuning and tests.
   int plan_per_sm = fp8 ? per_sm : 1;
   if (const char* env = std::getenv("PKV_PREFIX_CTAS_PER_SM")) {
     const long v = std::strtol(env, nullptr, 10);
