@@ -196,9 +196,10 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q
  *   PKV_ERR_WORKSPACE before anything is enqueued.
  *   The first call on a device looks up that device's copy of the array (with the device
  *   current); make that first call before any stream capture.
- *   All calls on a device share the one array and it keeps what the last call left; each
- *   call clears the part that must start at zero.  Two calls whose work can overlap on
- *   the GPU (different streams, or other devices' calls on this device) race on it.
+ *   All calls on a device share the one array, and it keeps what the last call left: it is
+ *   never cleared, and needs not be, since every value a call reads from it was written by
+ *   that same call.  Two calls whose work can overlap on the GPU (different streams, or
+ *   different host threads on one device) race on it.
  *   It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
  */
 pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const void* q,

@@ -227,9 +227,9 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         raise ValueError("out must be a contiguous [B, Hq, D] bfloat16 or float32 tensor")
     out_code = OUT_FP32 if out.dtype == torch.float32 else OUT_BF16
     sh = _stream(stream)
+    # a size query that fails leaves need at 0; the call below then makes the same check and
+    # raises with its status
     need = workspace_size(B, hq, desc.num_kv_heads, d, max_context_len) if B > 0 else 0
-    if B > 0 and need == 0 and lib.pkv_last_error():
-        raise PkvError(PKV_ERR_INVALID_ARG, lib.pkv_last_error().decode())
     ws_ptr, ws_bytes = None, 0
     if need > 0:
         ws = workspace if workspace is not None else _workspace(q.device, sh, need)
@@ -287,8 +287,6 @@ def cascade_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
                     max_members, max_prefix_len, seq_prefix.data_ptr())
     sh = _stream(stream)
     need = cascade_workspace_size(B, hq, desc.num_kv_heads, d, max_context_len, P, max_members, max_prefix_len)
-    if need == 0 and lib.pkv_last_error():
-        raise PkvError(PKV_ERR_INVALID_ARG, lib.pkv_last_error().decode())
     ws_ptr, ws_bytes = None, 0
     if need > 0:
         ws = workspace if workspace is not None else _workspace(q.device, sh, need)

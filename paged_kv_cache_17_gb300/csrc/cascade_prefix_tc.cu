@@ -49,6 +49,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "cascade.cuh"
 #include "mma_ops.cuh"
@@ -628,13 +629,15 @@ namespace {
 template <int D, bool FP8>
 int prefix_tc_configure(int device, cudaError_t* err) {
   using C = TcPrefixCfg<D, FP8>;
-  static int per_sm_of[64] = {};
+  // per device, set once; concurrent first calls may both compute it (the same value)
+  static std::atomic<int> per_sm_of[64] = {};
   *err = cudaSuccess;
   if (device < 0 || device >= 64) {
     *err = cudaErrorInvalidDevice;
     return 0;
   }
-  if (per_sm_of[device] > 0) return per_sm_of[device];
+  const int known = per_sm_of[device].load(std::memory_order_acquire);
+  if (known > 0) return known;
   auto kern = cascade_prefix_tc_kernel<D, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kBytes);
   // the largest shared-memory carveout, so that every CTA the shared memory can hold fits
@@ -661,8 +664,8 @@ int prefix_tc_configure(int device, cudaError_t* err) {
     *err = cudaErrorInvalidConfiguration;
     return 0;
   }
-  per_sm_of[device] = static_cast<int>(per_sm);
-  return per_sm_of[device];
+  per_sm_of[device].store(static_cast<int>(per_sm), std::memory_order_release);
+  return static_cast<int>(per_sm);
 }
 
 }  // namespace

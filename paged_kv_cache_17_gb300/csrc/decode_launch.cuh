@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "decode_kernel.cuh"
 #include "decode_mma.cuh"
 
@@ -38,11 +40,12 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
   using S = DecodeShape<D, FP8>;
   using C = DecodeCfg<D, G, FP8, S::kNWC, S::kStages>;
   auto kern = paged_decode_kernel<D, G, FP8, S::kNWC, S::kStages, CAS>;
-  static bool configured[64] = {};
-  if (device >= 0 && device < 64 && !configured[device]) {
+  // set once per device; concurrent first calls may both set it (the call is idempotent)
+  static std::atomic<bool> configured[64] = {};
+  if (device >= 0 && device < 64 && !configured[device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[device] = true;
+    configured[device].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -83,11 +86,12 @@ cudaError_t launch_decode_mma(const CUtensorMap& tk, const CUtensorMap& tv, cons
   using S = MmaShape<D, FP8>;
   using C = MmaCfg<D, G, FP8, S::kNWC, S::kStages>;
   auto kern = paged_decode_mma_kernel<D, G, FP8, S::kNWC, S::kStages, CAS>;
-  static bool configured[64] = {};
-  if (device >= 0 && device < 64 && !configured[device]) {
+  // set once per device; concurrent first calls may both set it (the call is idempotent)
+  static std::atomic<bool> configured[64] = {};
+  if (device >= 0 && device < 64 && !configured[device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[device] = true;
+    configured[device].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;

@@ -57,13 +57,17 @@ extern "C" pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* c
                                                          int32_t num_q_heads, int32_t max_context_len,
                                                          float softmax_scale, void* out, pkv_out_dtype out_dtype,
                                                          pkv_stream_t stream) {
-  if (!cache) return pkv_paged_decode_attention(cache, q, block_tables, max_blocks_per_seq, context_lens, batch,
-                                                num_q_heads, max_context_len, softmax_scale, out, out_dtype,
-                                                nullptr, 0, stream);  // reports the NULL descriptor
-  if (batch == 0) return PKV_OK;
+  // Without a usable descriptor, for an empty batch, or when the sizes themselves are
+  // refused, the regular entry point (given no workspace) makes the same checks and returns
+  // the same status and message as it would for this call; nothing is enqueued.
+  auto regular_without_workspace = [&]() {
+    return pkv_paged_decode_attention(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                                      max_context_len, softmax_scale, out, out_dtype, nullptr, 0, stream);
+  };
+  if (!cache || batch == 0) return regular_without_workspace();
   const size_t need = pkv_decode_workspace_size(batch, num_q_heads, cache->num_kv_heads, cache->head_dim,
                                                 max_context_len);
-  if (need == 0 && pkv_last_error()[0] != '\0') return PKV_ERR_INVALID_ARG;  // invalid sizes
+  if (need == 0 && pkv_last_error()[0] != '\0') return regular_without_workspace();
   if (need > kScratchBytes) {
     const std::string msg = "this call needs " + std::to_string(need) + " bytes of decode scratch; the "
                             "no-allocation entry point holds at most " + std::to_string(kScratchBytes) +

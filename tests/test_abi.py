@@ -110,3 +110,27 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(os.path, "exists", lambda p: False)
     with pytest.raises(ImportError):
         spec.loader.exec_module(mod)
+
+
+def test_noalloc_refusals_match_the_regular_entry_point_on_host(pkv):
+    """The entry point without a workspace refuses what the regular one refuses, with the
+    same status and message, before any CUDA call."""
+    cases = [
+        (dict(), dict(hq=12), pkv.PKV_ERR_UNSUPPORTED),                 # query group of 6
+        (dict(head_dim=96), dict(), pkv.PKV_ERR_UNSUPPORTED),           # head_dim not 64 / 128
+        (dict(block_size=8), dict(batch=0), pkv.PKV_ERR_UNSUPPORTED),   # bad pool, empty batch
+        (dict(), dict(hq=5), pkv.PKV_ERR_INVALID_ARG),                  # not a multiple of the kv heads
+        (dict(), dict(max_len=113), pkv.PKV_ERR_INVALID_ARG),           # beyond the table capacity
+        (dict(), dict(q=0x60008), pkv.PKV_ERR_INVALID_ARG),             # misaligned q
+        (dict(), dict(batch=0), pkv.PKV_OK),                            # empty batch: nothing to do
+    ]
+    for dkw, ckw, want in cases:
+        kw = dict(batch=4, hq=8, max_blocks=7, max_len=100, q=0x60000)
+        kw.update(ckw)
+        args = (ctypes.byref(desc(pkv, **dkw)), kw["q"], 0x80000, kw["max_blocks"], 0x90000, kw["batch"], kw["hq"],
+                kw["max_len"], 0.125, 0x70000, 0)
+        st_reg = pkv.lib.pkv_paged_decode_attention(*args, None, 0, None)
+        msg_reg = last(pkv)
+        st_na = pkv.lib.pkv_paged_decode_attention_noalloc(*args, None)
+        assert st_reg == want, (dkw, ckw, st_reg, msg_reg)
+        assert st_na == st_reg and last(pkv) == msg_reg, (dkw, ckw, st_na, last(pkv), msg_reg)
