@@ -62,6 +62,10 @@ def parse():
     ap.add_argument("--l2", choices=("flushed", "warm"), default="flushed",
                     help="flushed (default): L2 flushed between timed steps; warm: no flush, a diagnostic of "
                          "the reuse the shared-prefix and fork workloads get when a step follows a step")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="time only the --config workload, not the other target workloads next to it")
+    ap.add_argument("--no-read-ceiling", action="store_true",
+                    help="skip the read-only checksum pass that gives the ceiling of the decode's reads")
     ap.add_argument("--no-clock-fill", action="store_true",
                     help="do not run the untimed clock-sampling loop when the timed region is too short "
                          "(for profiler runs)")
@@ -260,6 +264,147 @@ def host_threads() -> int:
 
 # ------------------------------------------------------------------ our arm
 
+# the workloads timed next to the headline one, each with the decode call that suits it
+EXTRA_CONFIGS = (("long_context_70b", False), ("prefix_shared", True), ("fp8_fork", True))
+
+
+def config_dict(cfg, w: W.Workload, layout: str, cascade: bool, ws: int, cold: bool = True) -> dict:
+    """The workload description both arms print (nothing in it depends on the GPU)."""
+    B = w.batch
+    lens = cfg.len_range if cfg.kind == "uniform" else "mixed"
+    return {"workload": f"{cfg.name}: batch {B}, context {lens}, Hq {cfg.hq}, Hkv {cfg.hkv}, D {cfg.d}, block 16, "
+                        f"{cfg.kv_dtype} KV, append {w.slot_mapping.numel()} tokens",
+            "batch": B, "num_q_heads": cfg.hq, "num_kv_heads": cfg.hkv, "head_dim": cfg.d, "kv_dtype": cfg.kv_dtype,
+            "max_context_len": int(w.context_lens.max()), "total_context_tokens": w.total_tokens(),
+            "layout": layout, "decode_call": "cascade" if cascade else "paged",
+            "l2": ("flushed between timed steps: 256 MiB write, then a 256 MiB read of another buffer "
+                   "(both untimed; the read writes the dirty lines back before the step)") if cold else
+                  "warm: no flush between steps (diagnostic; each step finds the previous step's lines)",
+            "parallelism": f"replicas x{ws}"}
+
+
+class Timed:
+    """One workload resident on the device, its step (append + decode) and the timed loops
+    every measurement here shares: an untimed L2 flush and host-lead spin before each timed
+    step, CUDA events on the launching stream around it."""
+
+    def __init__(self, pkv, args, cfg, w: W.Workload, dev, cascade: bool):
+        self.pkv, self.args, self.cfg, self.w, self.dev = pkv, args, cfg, w, dev
+        B, hq, hkv, d = w.batch, cfg.hq, cfg.hkv, cfg.d
+        self.max_len = int(w.context_lens.max())
+        self.t = {k: (v.to(dev) if v is not None else None) for k, v in
+                  dict(q=w.q, k_cache=w.k_cache, v_cache=w.v_cache, k_new=w.k_new, v_new=w.v_new,
+                       slots=w.slot_mapping, tables=w.block_tables, lens=w.context_lens, scales=w.scales).items()}
+        self.out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=dev)
+        self.cas = w.cascade() if cascade else None
+        if self.cas is not None:
+            self.ct = {k: getattr(self.cas, k).to(dev) for k in ("prefix_tables", "prefix_lens", "member_indptr",
+                                                                 "member_seqs", "seq_prefix", "block_tables",
+                                                                 "context_lens")}
+            self.dec_len = max(16, int(self.cas.context_lens.max()))
+            need = pkv.cascade_workspace_size(B, hq, hkv, d, self.dec_len, self.cas.prefix_tables.shape[0],
+                                              self.cas.max_members, self.cas.max_prefix_len)
+        else:
+            self.dec_len = self.max_len
+            need = pkv.workspace_size(B, hq, hkv, d, self.max_len)
+        self.wsbuf = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
+        self.sums = torch.empty((B, hkv, 2), dtype=torch.int32, device=dev)
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.scrub = torch.zeros(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream()
+        self.cold = args.l2 == "flushed"
+
+    def decode(self, q, tables, lens, ctabs=None):
+        pkv, t, cfg = self.pkv, self.t, self.cfg
+        if self.cas is None:
+            pkv.paged_decode_attention(q, t["k_cache"], t["v_cache"], tables, lens, cfg.softmax_scale, self.out,
+                                       scales=t["scales"], max_context_len=self.max_len, workspace=self.wsbuf)
+        else:
+            c2 = ctabs or self.ct
+            pkv.cascade_decode_attention(q, t["k_cache"], t["v_cache"], c2["prefix_tables"], c2["prefix_lens"],
+                                         c2["member_indptr"], c2["member_seqs"], c2["seq_prefix"],
+                                         c2["block_tables"], c2["context_lens"], cfg.softmax_scale, self.out,
+                                         max_members=self.cas.max_members, max_prefix_len=self.cas.max_prefix_len,
+                                         max_context_len=self.dec_len, scales=t["scales"], workspace=self.wsbuf)
+
+    def step(self, mark=None):
+        t = self.t
+        self.pkv.paged_kv_append(t["k_new"], t["v_new"], t["slots"], t["k_cache"], t["v_cache"], scales=t["scales"])
+        if mark is not None:
+            mark.record(self.stream)
+        self.decode(t["q"], t["tables"], t["lens"])
+
+    def read_pass(self):
+        t = self.t
+        self.pkv.kv_checksum(t["k_cache"], t["v_cache"], t["tables"], t["lens"], self.sums, scales=t["scales"],
+                             max_context_len=self.max_len)
+
+    def evict(self, i):
+        if self.cold:
+            self.flush.fill_(i & 0xFF)  # evict the previous step's lines from L2 (not timed)
+
+    def lead(self):
+        # Untimed, between the L2 flush and the step: a read of a second buffer larger than
+        # L2, which writes back the flush's dirty lines and leaves L2 holding clean, unrelated
+        # lines (the timed kernel then pays for its own traffic only, as under ncu's cache
+        # control), then a GPU spin long enough for this Python host loop to queue the whole
+        # step before the GPU reaches it.
+        if self.cold:
+            self.scrub.amax()
+        torch.cuda._sleep(HOST_LEAD_CYCLES)
+
+    def warm(self, n):
+        for _ in range(n):
+            self.flush.fill_(1)
+            self.step()
+        torch.cuda.synchronize()
+        assert self.pkv.check_device_status() == 0
+
+    def timed(self, n, body, split_mark=False):
+        """Per-step milliseconds of `body` over n timed steps; with split_mark, the time from
+        a mark that the body records (between the append and the decode) to its end."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            self.evict(i)
+            self.lead()
+            if split_mark:
+                body(evs[i][0])
+            else:
+                evs[i][0].record(self.stream)
+                body()
+            evs[i][1].record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for (a, b) in evs]
+
+
+def summary_entry(tm: Timed, step_ms, dec_ms, read_ms, peak: float, ws: int, dev) -> dict:
+    """The per-workload figures: step and decode time, unique-byte GB/s and roofline
+    fractions, sequence-steps per second, and the read-only ceiling when it was timed."""
+    nb = step_bytes(tm.w)
+    B = tm.w.batch
+    step_tot = max_over_ranks(sum(step_ms), ws, dev)
+    dec_tot = max_over_ranks(sum(dec_ms), ws, dev)
+    n = len(step_ms)
+    dec_avg = dec_tot / n
+    achieved = nb["decode"] / (dec_avg * 1e-3) / 1e9
+    e = {"decode_call": "cascade" if tm.cas is not None else "paged", "batch": B,
+         "total_context_tokens": tm.w.total_tokens(), "unique_kv_bytes": nb["unique_kv"],
+         "decode_bytes": nb["decode"], "step_us": round(step_tot / n * 1e3, 2), "decode_us": round(dec_avg * 1e3, 2),
+         "decode_us_p10_p50_p90": [round(float(x) * 1e3, 2) for x in np.percentile(dec_ms, [10, 50, 90])],
+         "unique_kv_gbs": round(nb["unique_kv"] / (dec_avg * 1e-3) / 1e9, 1),
+         "decode_gbs": round(achieved, 1), "roofline_frac": round(achieved / peak, 4),
+         "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+         "seq_steps_per_s": round(B * ws * n / (step_tot * 1e-3), 1),
+         "decode_seq_steps_per_s": round(B * ws * n / (dec_tot * 1e-3), 1)}
+    if read_ms:
+        rd = max_over_ranks(sum(read_ms), ws, dev) / len(read_ms)
+        rbytes = nb["unique_kv"] + sum((s.length + 15) // 16 for s in tm.w.seqs) * 4 + B * 4
+        e["read_ceiling"] = {"us": round(rd * 1e3, 2), "gbs": round(rbytes / (rd * 1e-3) / 1e9, 1),
+                             "frac": round(rbytes / (rd * 1e-3) / 1e9 / peak, 4),
+                             "kernel": "kv_checksum_kernel (the decode's TMA gather, no arithmetic)"}
+    return e
+
+
 def run_ours(args):
     import paged_kv_cache_17_gb300 as pkv
 
@@ -270,69 +415,17 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     cfg = W.get(args.config)
     w = W.make_workload(cfg, seed=cfg.seed + 1000 * rank, layout=args.layout)
+    tm = Timed(pkv, args, cfg, w, dev, args.cascade)
     nb = step_bytes(w)
     B, hq, hkv, d = w.batch, cfg.hq, cfg.hkv, cfg.d
-    max_len = int(w.context_lens.max())
-    t = {k: (v.to(dev) if v is not None else None) for k, v in
-         dict(q=w.q, k_cache=w.k_cache, v_cache=w.v_cache, k_new=w.k_new, v_new=w.v_new, slots=w.slot_mapping,
-              tables=w.block_tables, lens=w.context_lens, scales=w.scales).items()}
-    out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=dev)
-    cas = w.cascade() if args.cascade else None
-    if cas is not None:
-        ct = {k: getattr(cas, k).to(dev) for k in ("prefix_tables", "prefix_lens", "member_indptr", "member_seqs",
-                                                    "seq_prefix", "block_tables", "context_lens")}
-        suffix_max = max(16, int(cas.context_lens.max()))
-        need = pkv.cascade_workspace_size(B, hq, hkv, d, suffix_max, cas.prefix_tables.shape[0], cas.max_members,
-                                          cas.max_prefix_len)
-    else:
-        need = pkv.workspace_size(B, hq, hkv, d, max_len)
-    wsbuf = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    scrub = torch.zeros(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+    max_len = tm.max_len
+    cas = tm.cas
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    peak = peak or FALLBACK_HBM_GBS
 
-    def decode(q, tables, lens, ctabs=None):
-        if cas is None:
-            pkv.paged_decode_attention(q, t["k_cache"], t["v_cache"], tables, lens, cfg.softmax_scale, out,
-                                       scales=t["scales"], max_context_len=max_len, workspace=wsbuf)
-        else:
-            c2 = ctabs or ct
-            pkv.cascade_decode_attention(q, t["k_cache"], t["v_cache"], c2["prefix_tables"], c2["prefix_lens"],
-                                         c2["member_indptr"], c2["member_seqs"], c2["seq_prefix"], c2["block_tables"],
-                                         c2["context_lens"], cfg.softmax_scale, out, max_members=cas.max_members,
-                                         max_prefix_len=cas.max_prefix_len, max_context_len=suffix_max,
-                                         scales=t["scales"], workspace=wsbuf)
-
-    def step(mark=None):
-        pkv.paged_kv_append(t["k_new"], t["v_new"], t["slots"], t["k_cache"], t["v_cache"], scales=t["scales"])
-        if mark is not None:
-            mark.record(stream)
-        decode(t["q"], t["tables"], t["lens"])
-
-    cold = args.l2 == "flushed"
-
-    def evict(i):
-        if cold:
-            flush.fill_(i & 0xFF)  # evict the previous step's lines from L2 (not timed)
-
-    def lead():
-        # Untimed, between the L2 flush and the step: a read of a second buffer larger than
-        # L2, which writes back the flush's dirty lines and leaves L2 holding clean, unrelated
-        # lines (the timed kernel then pays for its own traffic only, as under ncu's cache
-        # control), then a GPU spin long enough for this Python host loop to queue the whole
-        # step before the GPU reaches it.
-        if cold:
-            scrub.amax()
-        torch.cuda._sleep(HOST_LEAD_CYCLES)
-
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        step()
-    torch.cuda.synchronize()
-    assert pkv.check_device_status() == 0
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    dev_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
+    tm.warm(args.warmup)
     with ClockSampler(dev.index) as clk:
         if ws > 1:
             torch.distributed.barrier()
@@ -340,19 +433,9 @@ def run_ours(args):
         wall0 = time.perf_counter()
         # the step as a user runs it: append then decode, nothing in between (the decode's
         # launch overlaps the append's tail through programmatic dependent launch)
-        for i in range(args.steps):
-            evict(i)
-            lead()
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        # the decode kernel alone (the roofline figure): an event between append and decode
-        for i in range(args.steps):
-            evict(i)
-            lead()
-            step(mark=dev_evs[i][0])
-            dev_evs[i][1].record(stream)
-        torch.cuda.synchronize()
+        step_ms = tm.timed(args.steps, tm.step)
+        # the decode alone (the roofline figure): an event between append and decode
+        dec_ms = tm.timed(args.steps, lambda mark: tm.step(mark=mark), split_mark=True)
         if ws > 1:
             torch.distributed.barrier()
         wall = time.perf_counter() - wall0
@@ -364,35 +447,36 @@ def run_ours(args):
             t_end = time.perf_counter() + 0.5
             while time.perf_counter() < t_end:
                 for _ in range(50):
-                    flush.fill_(3)
-                    step()
+                    tm.flush.fill_(3)
+                    tm.step()
                 torch.cuda.synchronize()
         clocks = clk2.summary()
         clocks["window"] = "same step loop, 0.5 s right after the timed region (timed region too short)"
     else:
         clocks["window"] = "timed region"
-    step_ms = [a.elapsed_time(b) for (a, b) in evs]
-    dec_ms = [a.elapsed_time(b) for (a, b) in dev_evs]
-    tot_ms = sum(step_ms)
-    tot_ms = max_over_ranks(tot_ms, ws, dev)
+    # the read-only ceiling of the same gather (untimed warm-up, then the same protocol)
+    read_ms = []
+    if not args.no_read_ceiling and cas is None:
+        tm.read_pass()
+        torch.cuda.synchronize()
+        read_ms = tm.timed(args.steps, tm.read_pass)
     assert pkv.check_device_status() == 0
+    tot_ms = max_over_ranks(sum(step_ms), ws, dev)
     value = nb["step"] * ws * args.steps / (tot_ms * 1e-3) / 1e9
     ms_per_step = tot_ms / args.steps
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
-    achieved = nb["decode"] / (dec_avg_ms * 1e-3) / 1e9
-    peaks = measured_peaks()
-    peak = peaks.get("hbm_gbs")
-    peak_src = "measured" if peak else "fallback"
-    peak = peak or FALLBACK_HBM_GBS
+    head = summary_entry(tm, step_ms, dec_ms, read_ms, peak, ws, dev)
+    dec_avg_ms = head["decode_us"] * 1e-3
+    achieved = head["decode_gbs"]
 
     # our kernels per step: append, [prefix pass], decode, [merge: of split sequences, or of
     # the prefix records, which the tensor-core decode leaves to it]
-    dec_len = suffix_max if cas is not None else max_len
+    dec_len = tm.dec_len
     has_prefix = cas is not None and cas.prefix_tables.shape[0] > 0
     tensor_core = os.environ.get("PKV_DECODE_CUDA_CORES") != "1"
     deferred = has_prefix and tensor_core and os.environ.get("PKV_CASCADE_DEFER", "1") == "1"
     split = dec_len > pkv.partition_tokens(B, hkv, dec_len)
     launches_per_step = 2 + (1 if has_prefix else 0) + (1 if split or deferred else 0)
+    launches = launches_per_step * 2 * args.steps + len(read_ms)
 
     # ---- end to end through the public API with host buffers (pinned), H2D + D2H timed
     e2e = None
@@ -400,7 +484,7 @@ def run_ours(args):
         inputs = dict(q=w.q, k_new=w.k_new, v_new=w.v_new, slots=w.slot_mapping, tables=w.block_tables,
                       lens=w.context_lens)
         if cas is not None:
-            inputs.update({"c_" + k: getattr(cas, k) for k in ct})
+            inputs.update({"c_" + k: getattr(cas, k) for k in tm.ct})
         # the step's inputs staged in one pinned host buffer (256-byte aligned fields), copied
         # to the device in one transfer per step; the calls take device views into it
         offs, total = {}, 0
@@ -420,29 +504,56 @@ def run_ours(args):
 
         def e2e_step():
             d_pack.copy_(h_pack, non_blocking=True)
-            pkv.paged_kv_append(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], t["k_cache"], t["v_cache"],
-                                scales=t["scales"])
+            pkv.paged_kv_append(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], tm.t["k_cache"], tm.t["v_cache"],
+                                scales=tm.t["scales"])
             ctabs = {k[2:]: v for k, v in dev_in.items() if k.startswith("c_")} if cas is not None else None
-            decode(dev_in["q"], dev_in["tables"], dev_in["lens"], ctabs)
-            h_out.copy_(out, non_blocking=True)
+            tm.decode(dev_in["q"], dev_in["tables"], dev_in["lens"], ctabs)
+            h_out.copy_(tm.out, non_blocking=True)
 
         for _ in range(args.warmup):
             e2e_step()
         torch.cuda.synchronize()
-        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-        for i in range(args.steps):
-            evict(i)
-            lead()  # untimed, as for the device timing: the copies and kernels stay inside
-            ee[i][0].record(stream)
-            e2e_step()
-            ee[i][1].record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
-        e2e_ms = max_over_ranks(e2e_ms, ws, dev)
+        e2e_ms = max_over_ranks(sum(tm.timed(args.steps, e2e_step)), ws, dev)
         e2e = {"value": round(nb["step"] * ws * args.steps / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(e2e_ms / args.steps, 4)}
+               "ms_per_step": round(e2e_ms / args.steps, 4),
+               "seq_steps_per_s": round(B * ws * args.steps / (e2e_ms * 1e-3), 1)}
+        launches += launches_per_step * args.steps
+    head_partition = pkv.partition_tokens(B, hkv, max_len)
+    del tm
+    torch.cuda.empty_cache()
+
+    # ---- the other target workloads, the same protocol (decode call as suits each)
+    extras = {}
+    if not args.no_extra_configs:
+        for name, cascade in EXTRA_CONFIGS:
+            if name == args.config and cascade == args.cascade:
+                continue
+            xc = W.get(name)
+            xw = W.make_workload(xc, seed=xc.seed + 1000 * rank, layout=args.layout)
+            xt = Timed(pkv, args, xc, xw, dev, cascade)
+            xt.warm(args.warmup)
+            with ClockSampler(dev.index) as xclk:
+                x_step = xt.timed(args.steps, xt.step)
+                x_dec = xt.timed(args.steps, lambda mark: xt.step(mark=mark), split_mark=True)
+            x_read = []
+            if not args.no_read_ceiling and not cascade:
+                xt.read_pass()
+                torch.cuda.synchronize()
+                x_read = xt.timed(args.steps, xt.read_pass)
+            assert pkv.check_device_status() == 0
+            entry = summary_entry(xt, x_step, x_dec, x_read, peak, ws, dev)
+            entry["config"] = config_dict(xc, xw, args.layout, cascade, ws, xt.cold)
+            entry["partition_tokens"] = pkv.partition_tokens(xw.batch, xc.hkv, xt.dec_len)
+            xs = xclk.summary()
+            entry["clocks"] = {k: xs.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples")}
+            xsplit = xt.dec_len > entry["partition_tokens"]
+            xprefix = xt.cas is not None and xt.cas.prefix_tables.shape[0] > 0
+            xdefer = xprefix and tensor_core and os.environ.get("PKV_CASCADE_DEFER", "1") == "1"
+            launches += (2 + (1 if xprefix else 0) + (1 if xsplit or xdefer else 0)) * 2 * args.steps + len(x_read)
+            extras[name + ("_cascade" if cascade else "")] = entry
+            del xt
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -459,33 +570,31 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if cfg.kv_dtype == "bf16" else "e4m3",
         "data": f"synthetic (seeded N(0,1) bf16 q/K/V, {args.layout} 16-token block pool)",
-        "config": {"workload": f"{cfg.name}: batch {B}, context {cfg.len_range if cfg.kind == 'uniform' else 'mixed'}, "
-                               f"Hq {hq}, Hkv {hkv}, D {d}, block 16, {cfg.kv_dtype} KV, append {w.slot_mapping.numel()} tokens",
-                   "batch": B, "num_q_heads": hq, "num_kv_heads": hkv, "head_dim": d, "kv_dtype": cfg.kv_dtype,
-                   "max_context_len": max_len, "total_context_tokens": w.total_tokens(),
-                   "partition_tokens": pkv.partition_tokens(B, hkv, max_len),
-                   "layout": args.layout, "decode_call": "cascade" if cas is not None else "paged",
-                   "l2": ("flushed between timed steps: 256 MiB write, then a 256 MiB read of another buffer "
-                          "(both untimed; the read writes the dirty lines back before the step)") if cold else
-                         "warm: no flush between steps (diagnostic; each step finds the previous step's lines)",
-                   "parallelism": f"replicas x{ws}"},
+        "config": config_dict(cfg, w, args.layout, args.cascade, ws, args.l2 == "flushed"),
+        "partition_tokens": head_partition,
         "us_per_step": round(ms_per_step * 1e3, 2),
+        "seq_steps_per_s": round(B * ws * args.steps / (tot_ms * 1e-3), 1),
         "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
         "bytes_per_step": nb,
-        "decode_us": round(dec_avg_ms * 1e3, 2),
-        "decode_us_p10_p50_p90": [round(float(x) * 1e3, 2) for x in np.percentile(dec_ms, [10, 50, 90])],
+        "decode_us": head["decode_us"],
+        "decode_us_p10_p50_p90": head["decode_us_p10_p50_p90"],
+        "decode_seq_steps_per_s": head["decode_seq_steps_per_s"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None if cas is not None else ncu_traffic(cfg.name),
                      "kernel": decode_kernel_name(cfg, cas is not None),
                      "peak_source": f"{peak_src} hbm_gbs (copy)",
                      "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
+        "read_ceiling": head.get("read_ceiling"),
+        "configs": extras,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": launches_per_step * (3 if e2e is not None else 2) * args.steps,
+        "gpu_launches": launches,
         "timing": "step: events around append + decode (no event between them); decode_us: events around the "
-                  "decode alone, a second pass; e2e: events around one H2D copy of the step's inputs (staged in "
-                  "one pinned buffer) + append + decode + the D2H of the output, a third pass; each timed step "
-                  "follows an untimed L2 flush and an untimed GPU spin that lets the host queue the step first",
+                  "decode alone, a second pass; read_ceiling: events around the read-only checksum pass over the "
+                  "same tables; e2e: events around one H2D copy of the step's inputs (staged in one pinned "
+                  "buffer) + append + decode + the D2H of the output; each timed step follows an untimed L2 flush "
+                  "and an untimed GPU spin that lets the host queue the step first; configs: the other target "
+                  "workloads under the same protocol",
         "clocks": clocks,
         "wall_s": round(wall, 3),
     }
@@ -619,7 +728,7 @@ def run_reference(args):
     if rank != 0:
         return  # the oracle runs on rank 0 only
     cfg = W.get(args.config)
-    w = W.make_workload(cfg)
+    w = W.make_workload(cfg, layout=args.layout)
     thr = host_threads()
     per_step = max(1.0, min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -634,7 +743,10 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": cfg.name},
+        "data": f"synthetic (seeded N(0,1) bf16 q/K/V, {args.layout} 16-token block pool)",
+        "config": config_dict(cfg, w, args.layout, args.cascade, ws, args.l2 == "flushed"),
+        "timing": "the fp64 oracle on the host cores; each step a bounded sample of (sequence, kv head) groups "
+                  "of the workload (its attention is the same for the paged and the cascade call)",
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -270,6 +270,25 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
                                         pkv_stream_t stream);
 
 /*
+ * Checksum of the cached K and V of every (sequence, kv head), read through the block
+ * tables.  (The pages describe no such call.  It checks a pool's contents, e.g. after a
+ * block copy, and it is the decode's read pattern with nothing else: the same grid, TMA
+ * loads and partition length, so its time is the practical ceiling of the decode's reads.)
+ *   block_tables, max_blocks_per_seq, context_lens, batch, max_context_len: as for
+ *     pkv_paged_decode_attention (only the first ceil(context_lens[b] / 16) ids of row b
+ *     are read; out-of-range lengths are clamped and ids outside the pool read as zeros,
+ *     both flagged in the device status word).
+ *   checksums: device uint32 [batch][num_kv_heads][2], 4-byte aligned; entry [b][h][0]
+ *     covers K, [b][h][1] V.  With n = context_lens[b] and x_t the XOR of the 32-bit
+ *     little-endian words of row t of kv head h (head_dim elements as stored),
+ *       checksum = XOR over t = 0 .. n-1 of rotl32(x_t, t mod 32).
+ *   The call clears `checksums` on `stream` before it reads; batch == 0 is a no-op.
+ */
+pkv_status pkv_paged_kv_checksum(const pkv_cache_desc* cache, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                                 int32_t max_context_len, uint32_t* checksums, pkv_stream_t stream);
+
+/*
  * Read and clear the device status word of the current device after the work queued on
  * `stream` so far has finished (this call synchronises `stream`).  *flags receives the
  * PKV_DEVFLAG_* bits (may be NULL).  Returns PKV_ERR_DEVICE_CHECK if any bit was set,

@@ -44,7 +44,7 @@ EXPORTED_SYMBOLS = (
     "pkv_paged_kv_append", "pkv_decode_workspace_size",
     "pkv_decode_partition_tokens", "pkv_paged_decode_attention", "pkv_check_device_status",
     "pkv_status_string", "pkv_last_error", "pkv_version", "pkv_paged_decode_attention_noalloc",
-    "pkv_copy_blocks", "pkv_cascade_workspace_size", "pkv_cascade_decode_attention",
+    "pkv_copy_blocks", "pkv_cascade_workspace_size", "pkv_cascade_decode_attention", "pkv_paged_kv_checksum",
 )
 
 
@@ -90,6 +90,8 @@ def _load() -> ctypes.CDLL:
     lib.pkv_cascade_decode_attention.restype = ctypes.c_int
     lib.pkv_cascade_decode_attention.argtypes = [ctypes.POINTER(CacheDesc), P, ctypes.POINTER(PrefixDesc), P, i32, P,
                                                  i32, i32, i32, ctypes.c_float, P, ctypes.c_int, P, sz, P]
+    lib.pkv_paged_kv_checksum.restype = ctypes.c_int
+    lib.pkv_paged_kv_checksum.argtypes = [ctypes.POINTER(CacheDesc), P, i32, P, i32, i32, P, P]
     lib.pkv_copy_blocks.restype = ctypes.c_int
     lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(CacheDesc), P, i64, P]
     lib.pkv_check_device_status.restype = ctypes.c_int
@@ -296,6 +298,29 @@ def cascade_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: to
                                             B, hq, max_context_len, float(softmax_scale), out.data_ptr(),
                                             OUT_FP32 if out.dtype == torch.float32 else OUT_BF16, ws_ptr, ws_bytes,
                                             sh))
+    return out
+
+
+def kv_checksum(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                out: Optional[torch.Tensor] = None, *, scales: Optional[torch.Tensor] = None,
+                max_context_len: Optional[int] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Per (sequence, kv head) checksums of the cached K and V read through the block tables
+    (int32 [B, Hkv, 2]; the bits are the uint32 of include/pkv.h): a read-only pass with the
+    decode's gather, so its time is the ceiling of the decode's reads."""
+    desc = _cache_desc(k_cache, v_cache, None, scales)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if not (block_tables.is_contiguous() and context_lens.is_contiguous()) or block_tables.dim() != 2:
+        raise ValueError("block_tables must be a contiguous [B, max_blocks] and context_lens a contiguous [B]")
+    B = block_tables.shape[0]
+    if out is None:
+        out = torch.empty((B, desc.num_kv_heads, 2), dtype=torch.int32, device=k_cache.device)
+    if out.dtype != torch.int32 or tuple(out.shape) != (B, desc.num_kv_heads, 2) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous int32 tensor [B, num_kv_heads, 2]")
+    if max_context_len is None:
+        max_context_len = block_tables.shape[1] * desc.block_size
+    _check(lib.pkv_paged_kv_checksum(ctypes.byref(desc), block_tables.data_ptr(), block_tables.shape[1],
+                                     context_lens.data_ptr(), B, max_context_len, out.data_ptr(), _stream(stream)))
     return out
 
 

@@ -64,6 +64,12 @@ struct DecodeParams {
   int merge_warps;      // merge kernel: warps per query head (1, 2, 4 or 8; set by its launch)
   int defer_prefix;     // cascade: the decode writes a record for every prefixed sequence and
                         // the merge kernel combines it with the prefix records (tensor-core form)
+  // Failure-detection tests only (tensor-core form; 0 = off, the default): the consumer
+  // warps give up waiting for a K/V stage after this many cycles instead of about a second,
+  // and the producer warp waits this many cycles before its first load, so that the
+  // consumers' wait runs out while the loads are still to come.
+  long long test_consumer_wait_cycles;
+  long long test_producer_delay_cycles;
 };
 
 template <int D, int G, bool FP8, int NWC, int STAGES>

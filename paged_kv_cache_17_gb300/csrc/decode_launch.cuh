@@ -153,6 +153,22 @@ cudaError_t launch_copy_blocks(const int64_t* pairs, int64_t num_pairs, int64_t 
                                void* v_cache, int64_t num_blocks, uint32_t* status, int sm_count,
                                cudaStream_t stream);
 
+// read-only checksum pass over the cached K/V (kv_checksum.cu): grid (kv heads, batch,
+// partitions), the decode's tables, lengths and partition length
+struct ChecksumParams {
+  const int32_t* block_tables;  // [B][max_blocks]
+  const int32_t* context_lens;  // [B]
+  uint32_t* out;                // [B][Hkv][2], zeroed before the launch
+  uint32_t* status;
+  int max_blocks;
+  int hkv;
+  int num_blocks;
+  int max_context_len;
+  int split_blocks;
+};
+cudaError_t launch_kv_checksum(int row_bytes, const CUtensorMap& tk, const CUtensorMap& tv, const ChecksumParams& p,
+                               dim3 grid, cudaStream_t stream);
+
 // append (append.cu)
 cudaError_t launch_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
                           int hkv, int d, bool fp8, void* k_cache, void* v_cache, int64_t pool_slots,

@@ -77,6 +77,10 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   const int gid = lane >> 2, tig = lane & 3;
 
   if constexpr (!CAS) pdl_wait();
+  // The merge kernel that follows (launched with programmatic serialization) may be scheduled
+  // once every CTA of this grid has started: it then waits in griddepcontrol.wait for this
+  // grid to complete, with its launch and prologue already done instead of in the tail.
+  pdl_launch_dependents();
 
   int len = p.context_lens[b];
   // the first 32 block ids of this partition, loaded beside the length (the row has
@@ -183,6 +187,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
 
   if (warp == NWC) {
     // ================================================================ producer warp
+    if (p.test_producer_delay_cycles > 0) spin_cycles(p.test_producer_delay_cycles);
     int issued = 0;
     for (int base = 0; base < nloc && !timed_out; base += 32) {
       const int next = (base + 32 + lane < nloc) ? row[base + 32 + lane] : 0;  // prefetch
@@ -239,9 +244,10 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   if (warp < NWC) {
     // ================================================================ consumer warps
     const int mi = lane >> 3;
+    const long long wait_limit = p.test_consumer_wait_cycles > 0 ? p.test_consumer_wait_cycles : kWaitLimitCycles;
     for (int it = warp; it < nloc; it += NWC) {
       const int sg = it % STAGES;
-      if (!mbar_wait(&full_bar[sg], (it / STAGES) & 1)) {
+      if (!mbar_wait(&full_bar[sg], (it / STAGES) & 1, wait_limit)) {
         if (lane == 0) set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
         timed_out = true;
         break;

@@ -538,6 +538,15 @@ pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32
     if (const char* env = std::getenv("PKV_CASCADE_DEFER")) defer = env[0] == '1';
     p.defer_prefix = defer ? 1 : 0;
   }
+  // failure-detection tests: a short consumer wait and a late producer (tensor-core form)
+  if (const char* env = std::getenv("PKV_TEST_CONSUMER_WAIT_CYCLES")) {
+    const long long v = std::strtoll(env, nullptr, 10);
+    p.test_consumer_wait_cycles = v > 0 ? v : 0;
+  }
+  if (const char* env = std::getenv("PKV_TEST_PRODUCER_DELAY_CYCLES")) {
+    const long long v = std::strtoll(env, nullptr, 10);
+    p.test_producer_delay_cycles = v > 0 ? std::min(v, 100000000LL) : 0;  // at most about 50 ms
+  }
   int device = 0;
   cudaGetDevice(&device);
   const dim3 grid(static_cast<unsigned>(cache->num_kv_heads), static_cast<unsigned>(batch),
@@ -681,6 +690,53 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   return decode_common(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, max_context_len,
                        softmax_scale, out, out_dtype, workspace, workspace_bytes, stream, px->seq_prefix,
                        pp.pre_slots);
+}
+
+pkv_status pkv_paged_kv_checksum(const pkv_cache_desc* cache, const int32_t* block_tables,
+                                 int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                                 int32_t max_context_len, uint32_t* checksums, pkv_stream_t stream) {
+  t_last_error.clear();
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (batch < 0 || batch > 65535) return fail(PKV_ERR_INVALID_ARG, "batch must be in [0, 65535]");
+  if (batch == 0) return PKV_OK;
+  if (!block_tables || !context_lens || !checksums)
+    return fail(PKV_ERR_INVALID_ARG, "block_tables, context_lens and checksums must be non-NULL");
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4) || !aligned(checksums, 4))
+    return fail(PKV_ERR_INVALID_ARG, "block_tables, context_lens and checksums must be 4-byte aligned");
+  if (max_blocks_per_seq <= 0) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
+  if (max_context_len < 0) return fail(PKV_ERR_INVALID_ARG, "max_context_len must be >= 0");
+  if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * 16)
+    return fail(PKV_ERR_INVALID_ARG, "max_context_len %d exceeds max_blocks_per_seq * 16 = %lld", max_context_len,
+                static_cast<long long>(max_blocks_per_seq) * 16);
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != PKV_OK) return st;
+  const bool fp8 = cache->kv_dtype == PKV_KV_FP8_E4M3;
+  const Split sp = choose_split(batch, cache->num_kv_heads, max_context_len, dev->sm_count);
+  if (sp.max_splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "context too long for the partition grid");
+  CUtensorMap tk, tv;
+  if (!encode_kv_map(&tk, cache->k_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8) ||
+      !encode_kv_map(&tv, cache->v_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8))
+    return fail(PKV_ERR_INVALID_ARG, "cannot describe the KV pool as a TMA tensor map");
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t out_bytes = static_cast<size_t>(batch) * cache->num_kv_heads * 2 * sizeof(uint32_t);
+  cudaError_t e = cudaMemsetAsync(checksums, 0, out_bytes, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the checksums");
+  pkv::ChecksumParams p{};
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = checksums;
+  p.status = dev->status;
+  p.max_blocks = max_blocks_per_seq;
+  p.hkv = cache->num_kv_heads;
+  p.num_blocks = static_cast<int>(cache->num_blocks);
+  p.max_context_len = max_context_len;
+  p.split_blocks = sp.split_blocks;
+  const dim3 grid(static_cast<unsigned>(cache->num_kv_heads), static_cast<unsigned>(batch),
+                  static_cast<unsigned>(sp.max_splits));
+  e = pkv::launch_kv_checksum(cache->head_dim * (fp8 ? 1 : 2), tk, tv, p, grid, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "checksum launch");
+  return PKV_OK;
 }
 
 pkv_status pkv_check_device_status(pkv_stream_t stream, uint32_t* flags) {

@@ -61,16 +61,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false after the limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false after `limit` cycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long start = clock64();
   for (;;) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - start > kWaitLimitCycles) return false;
+    if (clock64() - start > limit) return false;
   }
+}
+
+// Spin for about `cycles` SM cycles (bounded by its argument).
+__device__ __forceinline__ void spin_cycles(long long cycles) {
+  const long long start = clock64();
+  while (clock64() - start < cycles) __nanosleep(256);
 }
 
 // ------------------------------------------------------------------ TMA

@@ -45,16 +45,43 @@ def check_contract(d, steps, warmup):
 
 
 def test_bench_line_plain_decode():
-    """Small workload: the plain decode with one partition per sequence (no merge kernel)."""
-    d = run_bench("--config", "tiny", "--steps", "5", "--warmup", "3", "--cpu-seconds", "1")
+    """Small workload: the plain decode with one partition per sequence (no merge kernel),
+    plus the read-only ceiling pass (one launch per timed step)."""
+    d = run_bench("--config", "tiny", "--steps", "5", "--warmup", "3", "--cpu-seconds", "1", "--no-extra-configs")
     check_contract(d, 5, 3)
-    assert d["gpu_launches"] == 2 * 3 * 5  # append + decode, three timed passes
+    assert d["gpu_launches"] == 2 * 3 * 5 + 5  # append + decode, three timed passes; the read pass
+    rc = d["read_ceiling"]
+    assert rc["us"] > 0 and rc["gbs"] > 0 and abs(rc["frac"] - rc["gbs"] / d["roofline"]["peak"]) < 1e-3
+    assert d["configs"] == {} and d["seq_steps_per_s"] > 0
 
 
 def test_bench_line_cascade():
     """Shared-prefix workload through the cascade call: append, prefix pass, decode and the
     merge kernel (bf16 pools merge the prefix records there)."""
-    d = run_bench("--config", "prefix_shared", "--cascade", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1")
+    d = run_bench("--config", "prefix_shared", "--cascade", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1",
+                  "--no-extra-configs")
     check_contract(d, 3, 3)
     assert d["gpu_launches"] == 4 * 3 * 3
     assert "cascade_prefix_tc_kernel" in d["roofline"]["kernel"]
+
+
+def test_bench_line_times_the_other_target_workloads():
+    """The default line also times the 70B-shaped long-context decode and both cascades under
+    the same protocol, each with its own roofline fraction and sequence-steps per second."""
+    d = run_bench("--config", "tiny", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1", "--no-e2e")
+    assert set(d["configs"]) == {"long_context_70b", "prefix_shared_cascade", "fp8_fork_cascade"}
+    for name, e in d["configs"].items():
+        for k in ("decode_us", "decode_us_p10_p50_p90", "unique_kv_gbs", "roofline_frac", "frac_of_8tbs",
+                  "seq_steps_per_s", "step_us", "config", "clocks"):
+            assert k in e, (name, k)
+        assert e["decode_us"] > 0 and 0 < e["roofline_frac"] < 2 and e["seq_steps_per_s"] > 0
+    assert "read_ceiling" in d["configs"]["long_context_70b"]
+    assert d["configs"]["fp8_fork_cascade"]["config"]["kv_dtype"] == "e4m3"
+
+
+def test_reference_arm_prints_the_same_config():
+    ours = run_bench("--config", "tiny", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1", "--no-extra-configs",
+                     "--no-e2e", "--no-read-ceiling")
+    ref = run_bench("--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "0", "--cpu-seconds", "1")
+    assert ref["impl"] == "reference" and ref["config"] == ours["config"]
+    assert ref["metric"] == ours["metric"] and ref["unit"] == ours["unit"]

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import assert_close
+from gpu_helpers import assert_close, e4m3_vmax, fp16_weight_atol
 
 pytestmark = pytest.mark.gpu
 
@@ -52,13 +52,13 @@ def env(**kv):
                 os.environ[k] = v
 
 
-def build(hkv, g, d, members, pblocks, seed, grow=0.0, no_own=0):
-    """`members` sequences share a prefix of `pblocks` blocks and own 1..40 tokens each (the
+def build(hkv, g, d, members, pblocks, seed, grow=0.0, no_own=0, own_range=(1, 40)):
+    """`members` sequences share a prefix of `pblocks` blocks and own `own_range` tokens each (the
     first `no_own` members none: the prefix is their whole context); with grow > 0 the K rows
     of prefix block j are multiplied by (1 + grow * j) before rounding to bf16, so later keys
     score higher and the running max climbs stage after stage."""
     gen = torch.Generator().manual_seed(seed)
-    own = torch.randint(1, 41, (members,), generator=gen).tolist()
+    own = torch.randint(own_range[0], own_range[1] + 1, (members,), generator=gen).tolist()
     own = [0] * no_own + own[no_own:]
     nb = pblocks + sum(W.blocks_for_tokens(n) for n in own) + 8
     pool = W.BlockPool(nb, generator=gen)
@@ -111,6 +111,7 @@ def test_tiles_and_long_splits(pkv, hkv, g, d, members, pblocks, split):
     ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
                             lens.numpy(), scale)
     assert_close(got, ref, "bf16", f"hkv={hkv} g={g} d={d} members={members} split={split}")
+    assert_close(got, ref, "fp32", f"hkv={hkv} g={g} d={d} members={members} split={split}")
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -122,6 +123,7 @@ def test_growing_scores_rescale(pkv, d):
     ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
                             lens.numpy(), scale)
     assert_close(got, ref, "bf16", f"growing scores d={d}")
+    assert_close(got, ref, "fp32", f"growing scores d={d}")
 
 
 @pytest.mark.parametrize("d,grow", [(128, 0.0), (64, 0.0), (128, 0.6)])
@@ -136,6 +138,7 @@ def test_e4m3_tiles_and_rescale(pkv, d, grow):
     ref = oracle.decode_all(W.bf16_bits(q), k8.numpy(), v8.numpy(), oracle.KV_E4M3, full.numpy(), lens.numpy(),
                             scale, scales=scales.numpy())
     assert_close(got, ref, "fp8", f"e4m3 d={d} grow={grow}")
+    assert_close(got, ref, fp16_weight_atol(e4m3_vmax(v8.numpy(), scales.numpy())), f"e4m3 d={d} grow={grow}, fp16 weights")
 
 
 def test_many_short_splits_are_capped(pkv):
@@ -148,6 +151,7 @@ def test_many_short_splits_are_capped(pkv):
     ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
                             lens.numpy(), scale)
     assert_close(got, ref, "bf16", "capped prefix splits")
+    assert_close(got, ref, "fp32", "capped prefix splits")
 
 
 @pytest.mark.parametrize("fp8", [False, True])
@@ -167,9 +171,40 @@ def test_merge_placement_and_prefix_occupancy(pkv, fp8, defer, per_sm):
         ref = oracle.decode_all(W.bf16_bits(q), k8.numpy(), v8.numpy(), oracle.KV_E4M3, full.numpy(), lens.numpy(),
                                 scale, scales=scales.numpy())
         assert_close(got, ref, "fp8", f"e4m3 defer={defer} per_sm={per_sm}")
+        assert_close(got, ref, fp16_weight_atol(e4m3_vmax(v8.numpy(), scales.numpy())),
+                     f"e4m3 defer={defer} per_sm={per_sm}, fp16 weights")
     else:
         with env(PKV_CASCADE_DEFER=defer, PKV_PREFIX_CTAS_PER_SM=per_sm, PKV_PREFIX_SPLIT_BLOCKS=8):
             got = run(pkv, c, kp.cuda(), vp.cuda(), q, scale)
         ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
                                 lens.numpy(), scale)
         assert_close(got, ref, "bf16", f"bf16 defer={defer} per_sm={per_sm}")
+        assert_close(got, ref, "fp32", f"bf16 defer={defer} per_sm={per_sm}")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("defer", ["0", "1"])
+def test_prefix_and_suffix_records_beyond_64(pkv, fp8, defer):
+    """16 prefix records (4-block splits of a 64-block prefix) plus 16-token partitions of
+    1,000-1,200 own tokens (63-75 partitions): 79-91 records per (sequence, kv head), past
+    the 64 whose (max, sum) pairs the merge kernel holds in lanes."""
+    c, kp, vp, q, full, lens = build(2, 4, 128, 5, 64, seed=1300 + int(fp8), own_range=(1000, 1200))
+    scale = 128 ** -0.5
+    knobs = dict(PKV_CASCADE_DEFER=defer, PKV_PREFIX_SPLIT_BLOCKS=4, PKV_SPLIT_TOKENS=16)
+    if fp8:
+        k8, ks = quant_e4m3(kp)
+        v8, vs = quant_e4m3(vp)
+        scales = torch.stack([ks, vs]).contiguous()
+        with env(**knobs):
+            got = run(pkv, c, k8.cuda(), v8.cuda(), q, scale, scales=scales)
+        ref = oracle.decode_all(W.bf16_bits(q), k8.numpy(), v8.numpy(), oracle.KV_E4M3, full.numpy(), lens.numpy(),
+                                scale, scales=scales.numpy())
+        assert_close(got, ref, "fp8", f"e4m3 records > 64, defer={defer}")
+        assert_close(got, ref, fp16_weight_atol(e4m3_vmax(v8.numpy(), scales.numpy())),
+                     f"e4m3 records > 64, defer={defer}, fp16 weights")
+    else:
+        with env(**knobs):
+            got = run(pkv, c, kp.cuda(), vp.cuda(), q, scale)
+        ref = oracle.decode_all(W.bf16_bits(q), W.bf16_bits(kp), W.bf16_bits(vp), oracle.KV_BF16, full.numpy(),
+                                lens.numpy(), scale)
+        assert_close(got, ref, "fp32", f"bf16 records > 64, defer={defer}")
