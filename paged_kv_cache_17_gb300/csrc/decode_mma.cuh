@@ -77,10 +77,6 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   const int gid = lane >> 2, tig = lane & 3;
 
   if constexpr (!CAS) pdl_wait();
-  // The merge kernel that follows (launched with programmatic serialization) may be scheduled
-  // once every CTA of this grid has started: it then waits in griddepcontrol.wait for this
-  // grid to complete, with its launch and prologue already done instead of in the tail.
-  pdl_launch_dependents();
 
   int len = p.context_lens[b];
   // the first 32 block ids of this partition, loaded beside the length (the row has

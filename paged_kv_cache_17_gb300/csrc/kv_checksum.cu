@@ -29,7 +29,8 @@ struct ChecksumCfg {
   static constexpr int kThreads = (NWC + 1) * 32;
   static constexpr int kBarOffset = 2 * kStages * kTile;
   static constexpr int kSmemBytes = 128 + kBarOffset + 2 * kStages * 8;  // 128: alignment slack
-  static constexpr int kChunksPerLane = RB / 32;          // 16-byte chunks of half a row
+  static constexpr int kChunksPerRow = RB / 16;           // 16-byte chunks of one row
+  static constexpr int kChunksPerLane = kTile / 16 / 32;  // of one tile, per lane
   static_assert(RB == 64 || RB == 128 || RB == 256, "row bytes");
   static_assert(kStages % NWC == 0, "each stage is always consumed by the same warp");
 };
@@ -115,8 +116,9 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   }
 
   // ------------------------------------------------------------------ consumer warps
-  // lane pair (2r, 2r + 1) folds row r of a tile, each lane half of the row's chunks
-  const int r = lane >> 1, half = lane & 1;
+  // Lane l folds chunks l, l + 32, ... of a tile: each load instruction of the warp reads
+  // 512 contiguous bytes (no bank conflicts).  rotl distributes over XOR, so every chunk
+  // enters the sum rotated by its row's position, with no per-row reduction.
   uint32_t kacc = 0, vacc = 0;
   for (int it = warp; it < nloc; it += NWC) {
     const int sg = it % STAGES;
@@ -124,24 +126,26 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       if (lane == 0) set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
       break;
     }
-    const uint4* kr = reinterpret_cast<const uint4*>(k_tiles + sg * C::kTile + r * RB) + half * C::kChunksPerLane;
-    const uint4* vr = reinterpret_cast<const uint4*>(v_tiles + sg * C::kTile + r * RB) + half * C::kChunksPerLane;
-    uint32_t xk = 0, xv = 0;
+    const uint4* kt = reinterpret_cast<const uint4*>(k_tiles + sg * C::kTile);
+    const uint4* vt = reinterpret_cast<const uint4*>(v_tiles + sg * C::kTile);
+    const int tok0 = (blk0 + it) * kBlockSize;
 #pragma unroll
-    for (int c = 0; c < C::kChunksPerLane; ++c) {
-      const uint4 a = kr[c], v = vr[c];
-      xk ^= a.x ^ a.y ^ a.z ^ a.w;
-      xv ^= v.x ^ v.y ^ v.z ^ v.w;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[sg]);  // the stage is read
-    xk ^= __shfl_xor_sync(kFull, xk, 1);
-    xv ^= __shfl_xor_sync(kFull, xv, 1);
-    const int t = (blk0 + it) * kBlockSize + r;
-    if (half == 0 && t < len) {
+    for (int i = 0; i < C::kChunksPerLane; ++i) {
+      const int j = i * 32 + lane;
+      const int t = tok0 + j / C::kChunksPerRow;
+      const uint4 a = kt[j], v = vt[j];
+      const uint32_t xk = t < len ? (a.x ^ a.y ^ a.z ^ a.w) : 0u;  // rows past the context: 0
+      const uint32_t xv = t < len ? (v.x ^ v.y ^ v.z ^ v.w) : 0u;
       kacc ^= rotl32(xk, t & 31);
       vacc ^= rotl32(xv, t & 31);
     }
+    // The stage goes back to the producer only after every value read from it has arrived
+    // in registers: the sums, which depend on all of them, are inputs of this statement, so
+    // neither the compiler nor the in-order issue can let the release below overtake a
+    // shared-memory load still in flight (the next TMA load into this stage would race it).
+    asm volatile("" ::"r"(kacc), "r"(vacc) : "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[sg]);
   }
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) {
