@@ -505,6 +505,9 @@ __global__ void __launch_bounds__((NWC + 1) * 32) __maxnreg__((DecodeRegCap<D, G
         consume_block<D, GW, FP8, true>(kt, vt, valid, smul, qd, rowoff, sig_g, sig_t, lane, pbuf, abuf, st);
       else
         consume_block<D, GW, FP8, false>(kt, vt, valid, smul, qd, rowoff, sig_g, sig_t, lane, pbuf, abuf, st);
+      // read through the generic proxy, refilled by TMA (async proxy): order the reads first
+      fence_proxy_async_smem();
+      __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[sg]);
     }
   }

@@ -273,6 +273,7 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
                        "r"(h1), "r"(h2), "r"(h3)
                        : "memory");
         }
+        fence_proxy_async_smem();  // the codes were read through the generic proxy; TMA refills the slot
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[sg]);  // the ring slot is free again
         kb = kc;
@@ -333,6 +334,10 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         mma16<FP8>(o[mt], a0, a1, a2, a3, bh0, bh1);
         mma16<FP8>(o[mt], a0, a1, a2, a3, bl0, bl1);
       }
+      // The ring tiles were read with ldmatrix (generic proxy) and the producer refills them
+      // with TMA (async proxy): without this fence the refill can land while a read of the
+      // stage is still pending (seen as wrong output dims in repeated runs).
+      if constexpr (!FP8) fence_proxy_async_smem();
       __syncwarp();  // the tiles are read (E4M3: this warp's fp16 tiles are rewritten next)
       if (!FP8 && lane == 0) mbar_arrive(&empty_bar[sg]);
     }

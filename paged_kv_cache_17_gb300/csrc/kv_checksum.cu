@@ -139,11 +139,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       kacc ^= rotl32(xk, t & 31);
       vacc ^= rotl32(xv, t & 31);
     }
-    // The stage goes back to the producer only after every value read from it has arrived
-    // in registers: the sums, which depend on all of them, are inputs of this statement, so
-    // neither the compiler nor the in-order issue can let the release below overtake a
-    // shared-memory load still in flight (the next TMA load into this stage would race it).
-    asm volatile("" ::"r"(kacc), "r"(vacc) : "memory");
+    // The stage goes back to the producer only once its reads are ordered before the next
+    // TMA load into it: they went through the generic proxy, the refill goes through the
+    // async proxy, so a proxy fence is needed (without it the refill could land under a read
+    // still pending and the sums came out wrong when stages were reused).
+    fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[sg]);
   }

@@ -271,3 +271,14 @@ def test_workspace_needs_no_initialisation():
             pkv.paged_decode_attention(t["q"], t["k_cache"], t["v_cache"], t["block_tables"], t["context_lens"],
                                        w.cfg.softmax_scale, out, max_context_len=4096, workspace=small)
     assert ei.value.status == pkv.PKV_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "fp8_fork"])
+def test_repeated_decodes_give_identical_bits(name):
+    """Ten plain decodes back to back on the same inputs give the same bits (the ring's
+    generic-proxy reads are fenced before TMA refills their stage)."""
+    w = W.make_workload(name)
+    t = to_dev(w)
+    outs = [gpu_step(w, append=False, t=t)[1].cpu() for _ in range(10)]
+    assert all(torch.equal(o, outs[0]) for o in outs[1:]), "repeated decodes differ"
+    _check_flags()
