@@ -334,6 +334,23 @@ class Timed:
             mark.record(self.stream)
         self.decode(t["q"], t["tables"], t["lens"])
 
+    def fused_step(self, inputs=None):
+        """The step in one call (append fused into the decode; plain decode only)."""
+        t = self.t
+        i = inputs or dict(k_new=t["k_new"], v_new=t["v_new"], slots=t["slots"], q=t["q"], tables=t["tables"],
+                           lens=t["lens"])
+        self.pkv.paged_append_decode(i["k_new"], i["v_new"], i["slots"], i["q"], t["k_cache"], t["v_cache"],
+                                     i["tables"], i["lens"], self.cfg.softmax_scale, self.out, scales=t["scales"],
+                                     max_context_len=self.max_len, workspace=self.wsbuf)
+
+    def user_step(self):
+        """The step as a user runs it: the fused call for the plain decode, append then the
+        cascade call for shared prefixes."""
+        if self.cas is None:
+            self.fused_step()
+        else:
+            self.step()
+
     def read_pass(self):
         t = self.t
         self.pkv.kv_checksum(t["k_cache"], t["v_cache"], t["tables"], t["lens"], self.sums, scales=t["scales"],
@@ -357,6 +374,8 @@ class Timed:
         for _ in range(n):
             self.flush.fill_(1)
             self.step()
+            if self.cas is None:
+                self.fused_step()
         torch.cuda.synchronize()
         assert self.pkv.check_device_status() == 0
 
@@ -431,11 +450,13 @@ def run_ours(args):
             torch.distributed.barrier()
         torch.cuda.synchronize()
         wall0 = time.perf_counter()
-        # the step as a user runs it: append then decode, nothing in between (the decode's
-        # launch overlaps the append's tail through programmatic dependent launch)
-        step_ms = tm.timed(args.steps, tm.step)
-        # the decode alone (the roofline figure): an event between append and decode
+        # the step as a user runs it: one call that appends each sequence's new token and
+        # decodes (the cascade: append, then the cascade call)
+        step_ms = tm.timed(args.steps, tm.user_step)
+        # the decode alone (the roofline figure): the two calls with an event between them
         dec_ms = tm.timed(args.steps, lambda mark: tm.step(mark=mark), split_mark=True)
+        # the two calls back to back, for comparison with the fused step
+        two_call_ms = tm.timed(args.steps, tm.step) if cas is None else step_ms
         if ws > 1:
             torch.distributed.barrier()
         wall = time.perf_counter() - wall0
@@ -448,7 +469,7 @@ def run_ours(args):
             while time.perf_counter() < t_end:
                 for _ in range(50):
                     tm.flush.fill_(3)
-                    tm.step()
+                    tm.user_step()
                 torch.cuda.synchronize()
         clocks = clk2.summary()
         clocks["window"] = "same step loop, 0.5 s right after the timed region (timed region too short)"
@@ -469,14 +490,18 @@ def run_ours(args):
     achieved = head["decode_gbs"]
 
     # our kernels per step: append, [prefix pass], decode, [merge: of split sequences, or of
-    # the prefix records, which the tensor-core decode leaves to it]
+    # the prefix records, which the tensor-core decode leaves to it]; the fused step has no
+    # separate append (the CUDA-core form runs the two calls)
     dec_len = tm.dec_len
     has_prefix = cas is not None and cas.prefix_tables.shape[0] > 0
     tensor_core = os.environ.get("PKV_DECODE_CUDA_CORES") != "1"
     deferred = has_prefix and tensor_core and os.environ.get("PKV_CASCADE_DEFER", "1") == "1"
     split = dec_len > pkv.partition_tokens(B, hkv, dec_len)
     launches_per_step = 2 + (1 if has_prefix else 0) + (1 if split or deferred else 0)
-    launches = launches_per_step * 2 * args.steps + len(read_ms)
+    user_launches = launches_per_step - (1 if cas is None and tensor_core else 0)
+    launches = user_launches * args.steps + launches_per_step * args.steps + len(read_ms)
+    if cas is None:
+        launches += launches_per_step * args.steps  # the two-call comparison pass
 
     # ---- end to end through the public API with host buffers (pinned), H2D + D2H timed
     e2e = None
@@ -504,10 +529,13 @@ def run_ours(args):
 
         def e2e_step():
             d_pack.copy_(h_pack, non_blocking=True)
-            pkv.paged_kv_append(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], tm.t["k_cache"], tm.t["v_cache"],
-                                scales=tm.t["scales"])
-            ctabs = {k[2:]: v for k, v in dev_in.items() if k.startswith("c_")} if cas is not None else None
-            tm.decode(dev_in["q"], dev_in["tables"], dev_in["lens"], ctabs)
+            if cas is None:
+                tm.fused_step(dev_in)
+            else:
+                pkv.paged_kv_append(dev_in["k_new"], dev_in["v_new"], dev_in["slots"], tm.t["k_cache"],
+                                    tm.t["v_cache"], scales=tm.t["scales"])
+                ctabs = {k[2:]: v for k, v in dev_in.items() if k.startswith("c_")}
+                tm.decode(dev_in["q"], dev_in["tables"], dev_in["lens"], ctabs)
             h_out.copy_(tm.out, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -518,7 +546,7 @@ def run_ours(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e2e_ms / args.steps, 4),
                "seq_steps_per_s": round(B * ws * args.steps / (e2e_ms * 1e-3), 1)}
-        launches += launches_per_step * args.steps
+        launches += user_launches * args.steps
     head_partition = pkv.partition_tokens(B, hkv, max_len)
     del tm
     torch.cuda.empty_cache()
@@ -534,7 +562,7 @@ def run_ours(args):
             xt = Timed(pkv, args, xc, xw, dev, cascade)
             xt.warm(args.warmup)
             with ClockSampler(dev.index) as xclk:
-                x_step = xt.timed(args.steps, xt.step)
+                x_step = xt.timed(args.steps, xt.user_step)
                 x_dec = xt.timed(args.steps, lambda mark: xt.step(mark=mark), split_mark=True)
             x_read = []
             if not args.no_read_ceiling and not cascade:
@@ -550,7 +578,9 @@ def run_ours(args):
             xsplit = xt.dec_len > entry["partition_tokens"]
             xprefix = xt.cas is not None and xt.cas.prefix_tables.shape[0] > 0
             xdefer = xprefix and tensor_core and os.environ.get("PKV_CASCADE_DEFER", "1") == "1"
-            launches += (2 + (1 if xprefix else 0) + (1 if xsplit or xdefer else 0)) * 2 * args.steps + len(x_read)
+            x_per_step = 2 + (1 if xprefix else 0) + (1 if xsplit or xdefer else 0)
+            x_user = x_per_step - (1 if xt.cas is None and tensor_core else 0)
+            launches += (x_user + x_per_step) * args.steps + len(x_read)
             extras[name + ("_cascade" if cascade else "")] = entry
             del xt
             torch.cuda.empty_cache()
@@ -573,6 +603,9 @@ def run_ours(args):
         "config": config_dict(cfg, w, args.layout, args.cascade, ws, args.l2 == "flushed"),
         "partition_tokens": head_partition,
         "us_per_step": round(ms_per_step * 1e3, 2),
+        "step_call": "paged_append_decode (one call: the append fused into the decode)" if cas is None else
+                     "paged_kv_append + cascade_decode_attention",
+        "two_call_step_us": round(max_over_ranks(sum(two_call_ms), ws, dev) / args.steps * 1e3, 2),
         "seq_steps_per_s": round(B * ws * args.steps / (tot_ms * 1e-3), 1),
         "frac_of_8tbs": round(value / NOMINAL_HBM_GBS, 4),
         "bytes_per_step": nb,
@@ -589,8 +622,9 @@ def run_ours(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": launches,
-        "timing": "step: events around append + decode (no event between them); decode_us: events around the "
-                  "decode alone, a second pass; read_ceiling: events around the read-only checksum pass over the "
+        "timing": "step: events around the step as a user runs it (the fused append + decode call; cascades: "
+                  "append, then the cascade call); two_call_step_us: events around append + decode as two calls; "
+                  "decode_us: events around the decode alone (the two calls with an event between them); read_ceiling: events around the read-only checksum pass over the "
                   "same tables; e2e: events around one H2D copy of the step's inputs (staged in one pinned "
                   "buffer) + append + decode + the D2H of the output; each timed step follows an untimed L2 flush "
                   "and an untimed GPU spin that lets the host queue the step first; configs: the other target "

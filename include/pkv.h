@@ -186,6 +186,35 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q
                                       pkv_stream_t stream);
 
 /*
+ * One decode step in one launch: the append of pkv_paged_kv_append and the attention of
+ * pkv_paged_decode_attention, for the shape of a decode step -- one new token per sequence,
+ * token b being sequence b's token at position context_lens[b] - 1 (section 1: each step
+ * computes K, V of the new token only, appends them, and attends over the cache that now
+ * holds it; section 4 worked example: token 1025 goes to the next slot of the sequence's
+ * last block).
+ *   k, v: [batch][num_kv_heads][head_dim] bf16, 16-byte aligned: the new token of each
+ *     sequence.  slot_mapping: [batch] int64, 8-byte aligned: the slot of that token, which
+ *     must be the slot of position context_lens[b] - 1 in row b of block_tables; < 0: the
+ *     sequence appends nothing this step (its attention still runs over the pool as it is).
+ *   Everything else as for pkv_paged_decode_attention.
+ *   Result: the pool and out are bit for bit those of pkv_paged_kv_append(cache, k, v,
+ *   slot_mapping, batch) followed by pkv_paged_decode_attention(...) on the same stream.
+ *   The tensor-core form stores each new token from the CTA that reads the sequence's last
+ *   block and writes it into that CTA's copy of the block, so no separate launch and no
+ *   re-read is needed.  A slot that is not position context_lens[b] - 1 of the table (or is
+ *   outside the pool) sets PKV_DEVFLAG_BAD_SLOT; an in-pool one is stored, but the decode
+ *   then reads that block as the pool held it before this call.  A sequence with
+ *   context_lens[b] == 0 appends nothing.  With PKV_DECODE_CUDA_CORES=1 the two calls run
+ *   one after the other.
+ */
+pkv_status pkv_paged_append_decode(const pkv_cache_desc* cache, const void* k, const void* v,
+                                   const int64_t* slot_mapping, const void* q, const int32_t* block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                                   int32_t num_q_heads, int32_t max_context_len, float softmax_scale, void* out,
+                                   pkv_out_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                   pkv_stream_t stream);
+
+/*
  * Decode attention without a caller-provided workspace.  (The pages describe no such
  * call; it serves callers that cannot allocate device memory when they run a decode step:
  * an allocator that has reserved all device memory for itself, a serving loop that

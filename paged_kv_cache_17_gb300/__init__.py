@@ -45,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "pkv_decode_partition_tokens", "pkv_paged_decode_attention", "pkv_check_device_status",
     "pkv_status_string", "pkv_last_error", "pkv_version", "pkv_paged_decode_attention_noalloc",
     "pkv_copy_blocks", "pkv_cascade_workspace_size", "pkv_cascade_decode_attention", "pkv_paged_kv_checksum",
+    "pkv_paged_append_decode",
 )
 
 
@@ -90,6 +91,9 @@ def _load() -> ctypes.CDLL:
     lib.pkv_cascade_decode_attention.restype = ctypes.c_int
     lib.pkv_cascade_decode_attention.argtypes = [ctypes.POINTER(CacheDesc), P, ctypes.POINTER(PrefixDesc), P, i32, P,
                                                  i32, i32, i32, ctypes.c_float, P, ctypes.c_int, P, sz, P]
+    lib.pkv_paged_append_decode.restype = ctypes.c_int
+    lib.pkv_paged_append_decode.argtypes = [ctypes.POINTER(CacheDesc), P, P, P, P, P, i32, P, i32, i32, i32,
+                                            ctypes.c_float, P, ctypes.c_int, P, sz, P]
     lib.pkv_paged_kv_checksum.restype = ctypes.c_int
     lib.pkv_paged_kv_checksum.argtypes = [ctypes.POINTER(CacheDesc), P, i32, P, i32, i32, P, P]
     lib.pkv_copy_blocks.restype = ctypes.c_int
@@ -239,6 +243,51 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     _check(lib.pkv_paged_decode_attention(ctypes.byref(desc), q.data_ptr(), block_tables.data_ptr(), max_blocks,
                                           context_lens.data_ptr(), B, hq, max_context_len, float(softmax_scale),
                                           out.data_ptr(), out_code, ws_ptr, ws_bytes, sh))
+    return out
+
+
+def paged_append_decode(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, q: torch.Tensor,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                        context_lens: torch.Tensor, softmax_scale: float, out: Optional[torch.Tensor] = None, *,
+                        scales: Optional[torch.Tensor] = None, max_context_len: Optional[int] = None,
+                        workspace: Optional[torch.Tensor] = None,
+                        stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Append each sequence's new token (k, v [B, Hkv, D] bf16 at slot_mapping [B] int64, the
+    slot of position context_lens[b] - 1) and run decode attention over the cache that holds
+    it, in one launch; the same pool and output as paged_kv_append then paged_decode_attention."""
+    desc = _cache_desc(k_cache, v_cache, None, scales)
+    if q.dtype != torch.bfloat16 or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be a contiguous bfloat16 tensor [B, Hq, D]")
+    B, hq, d = q.shape
+    if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16 or not (k.is_contiguous() and v.is_contiguous()):
+        raise TypeError("k and v must be contiguous bfloat16")
+    if tuple(k.shape) != (B, desc.num_kv_heads, desc.head_dim) or k.shape != v.shape:
+        raise ValueError("k, v must be [B, num_kv_heads, head_dim]: one new token per sequence")
+    if slot_mapping.dtype != torch.int64 or tuple(slot_mapping.shape) != (B,) or not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be a contiguous int64 tensor [B]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if not (block_tables.is_contiguous() and context_lens.is_contiguous()):
+        raise ValueError("block_tables and context_lens must be contiguous")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("block_tables must be [B, max_blocks] and context_lens [B]")
+    max_blocks = block_tables.shape[1]
+    if max_context_len is None:
+        max_context_len = max_blocks * desc.block_size
+    if out is None:
+        out = torch.empty((B, hq, d), dtype=torch.bfloat16, device=q.device)
+    if out.dtype not in (torch.bfloat16, torch.float32) or tuple(out.shape) != (B, hq, d) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B, Hq, D] bfloat16 or float32 tensor")
+    sh = _stream(stream)
+    need = workspace_size(B, hq, desc.num_kv_heads, d, max_context_len) if B > 0 else 0
+    ws_ptr, ws_bytes = None, 0
+    if need > 0:
+        ws = workspace if workspace is not None else _workspace(q.device, sh, need)
+        ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    _check(lib.pkv_paged_append_decode(ctypes.byref(desc), k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(),
+                                       q.data_ptr(), block_tables.data_ptr(), max_blocks, context_lens.data_ptr(), B,
+                                       hq, max_context_len, float(softmax_scale), out.data_ptr(),
+                                       OUT_FP32 if out.dtype == torch.float32 else OUT_BF16, ws_ptr, ws_bytes, sh))
     return out
 
 

@@ -45,21 +45,8 @@ __global__ void __launch_bounds__(256) paged_append_kernel(const uint4* __restri
   } else {
     const float ks = scales[h];
     const float vs = scales[hkv + h];
-    auto quant = [](uint4 w, float sc) {
-      const uint32_t in[4] = {w.x, w.y, w.z, w.w};
-      uint32_t outw[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const float a0 = __fdiv_rn(bf16_lo(in[2 * j]), sc), a1 = __fdiv_rn(bf16_hi(in[2 * j]), sc);
-        const float a2 = __fdiv_rn(bf16_lo(in[2 * j + 1]), sc), a3 = __fdiv_rn(bf16_hi(in[2 * j + 1]), sc);
-        const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
-        const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a2, a3), __NV_SATFINITE, __NV_E4M3);
-        outw[j] = (lo & 0xffffu) | (hi << 16);
-      }
-      return make_uint2(outw[0], outw[1]);
-    };
-    reinterpret_cast<uint2*>(k_cache)[row * pieces_per_row + c] = quant(kw, ks);
-    reinterpret_cast<uint2*>(v_cache)[row * pieces_per_row + c] = quant(vw, vs);
+    reinterpret_cast<uint2*>(k_cache)[row * pieces_per_row + c] = e4m3_quant8(kw, ks);
+    reinterpret_cast<uint2*>(v_cache)[row * pieces_per_row + c] = e4m3_quant8(vw, vs);
   }
 }
 

@@ -70,6 +70,16 @@ struct DecodeParams {
   // consumers' wait runs out while the loads are still to come.
   long long test_consumer_wait_cycles;
   long long test_producer_delay_cycles;
+  // Fused append (tensor-core form, plain decode): sequence b's new token, at position
+  // context_lens[b] - 1, is k_new / v_new [B][Hkv][D] bf16 for slot new_slots[b] (< 0: none);
+  // the CTA holding the sequence's last block writes it into the pool (k_pool / v_pool) and
+  // into its copy of that block.  fused == 0: none of this.
+  int fused;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int64_t* new_slots;
+  void* k_pool;
+  void* v_pool;
 };
 
 template <int D, int G, bool FP8, int NWC, int STAGES>

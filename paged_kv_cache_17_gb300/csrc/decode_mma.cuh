@@ -130,6 +130,43 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
   }
   const int nloc = min(nblk, blk0 + p.split_blocks) - blk0;
 
+  // Fused append: the CTA holding sequence b's last block stores the step's new token (kv
+  // head h) into the pool -- what the append kernel would store -- and writes it into its
+  // copy of that block before reading it, so the block need not be re-read after the store.
+  // A slot that is not position len - 1 of the sequence's table is stored but not patched in
+  // (the decode then reads the pool as the TMA found it) and flagged.
+  constexpr int kRowChunks = D / 8;  // 16-byte chunks of a bf16 row
+  int patch_it = -1;                 // local index of the block to patch
+  uint4 newrow = make_uint4(0u, 0u, 0u, 0u);  // lanes < 2 kRowChunks: chunk (lane mod kRowChunks)
+                                              // of the new K (lane < kRowChunks) or V row, as stored
+  if constexpr (!CAS) {
+    if (p.fused && (nblk - 1) / p.split_blocks == s) {
+      const int64_t slot = p.new_slots[b];
+      if (slot >= 0) {
+        const int lastit = nblk - 1 - blk0;
+        const int64_t want = static_cast<int64_t>(p.block_tables[static_cast<size_t>(b) * p.max_blocks + nblk - 1]) *
+                                 kBlockSize + (len - 1) % kBlockSize;
+        const bool in_pool = slot < static_cast<int64_t>(p.num_blocks) * kBlockSize;
+        if (warp == lastit % NWC && lane < 2 * kRowChunks) {
+          const bool isv = lane >= kRowChunks;
+          const int c = lane % kRowChunks;
+          const size_t src = (static_cast<size_t>(b) * p.hkv + h) * kRowChunks + c;
+          newrow = reinterpret_cast<const uint4*>(isv ? p.v_new : p.k_new)[src];
+          const size_t dst = (static_cast<size_t>(slot) * p.hkv + h) * kRowChunks + c;
+          if constexpr (FP8) {
+            const uint2 code = e4m3_quant8(newrow, p.scales[(isv ? p.hkv : 0) + h]);
+            newrow = make_uint4(code.x, code.y, 0u, 0u);
+            if (in_pool) reinterpret_cast<uint2*>(isv ? p.v_pool : p.k_pool)[dst] = code;
+          } else {
+            if (in_pool) reinterpret_cast<uint4*>(isv ? p.v_pool : p.k_pool)[dst] = newrow;
+          }
+        }
+        if (slot == want && in_pool) patch_it = lastit;
+        else if (threadIdx.x == 0) set_flag(p.status, PKV_DEVFLAG_BAD_SLOT);
+      }
+    }
+  }
+
   // q as the B operand of the score product: column n = head gid of the group (zero
   // columns past G), k = head_dim; one pair of bf16 words per k-step
   uint32_t qb[KS][2];
@@ -251,6 +288,21 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       uint32_t kb = smem_u32(k_tiles + sg * C::kRingTile);
       uint32_t vb = smem_u32(v_tiles + sg * C::kRingTile);
       const int valid = min(kBlockSize, len - (blk0 + it) * kBlockSize);  // >= 1
+      if (it == patch_it) {  // fused append: the new token's row (valid - 1) of this block
+        if (lane < 2 * kRowChunks) {
+          const bool isv = lane >= kRowChunks;
+          const int c = lane % kRowChunks;
+          if constexpr (FP8) {  // the raw codes, before this warp expands them
+            uint8_t* rowp = (isv ? v_tiles : k_tiles) + sg * C::kRingTile + (valid - 1) * D + c * 8;
+            *reinterpret_cast<uint2*>(rowp) = make_uint2(newrow.x, newrow.y);
+          } else {
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz_addr<D>(isv ? vb : kb, valid - 1, c)),
+                         "r"(newrow.x), "r"(newrow.y), "r"(newrow.z), "r"(newrow.w)
+                         : "memory");
+          }
+        }
+        __syncwarp();
+      }
       if constexpr (FP8) {
         // expand both tiles into this warp's fp16 tiles: 8 codes -> one swizzled 16-byte chunk
         const uint32_t kc = smem_u32(smem + C::kRingBytes + warp * 2 * C::kTileBytes);

@@ -460,14 +460,22 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num
 
 namespace {
 
+// The step's new tokens for the fused append of the decode (one per sequence).
+struct FusedAppend {
+  const void* k;
+  const void* v;
+  const int64_t* slots;
+};
+
 // Validation and launch shared by the plain and the cascade decode: the decode kernel over
 // each sequence's own blocks, merging pre_slots shared-prefix records per (b, h) for the
-// sequences that seq_prefix marks (none when seq_prefix is NULL).
+// sequences that seq_prefix marks (none when seq_prefix is NULL); with `fused`, the decode
+// kernel also appends each sequence's new token (tensor-core form, plain decode only).
 pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32_t* block_tables,
                          int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch, int32_t num_q_heads,
                          int32_t max_context_len, float softmax_scale, void* out, pkv_out_dtype out_dtype,
                          void* workspace, size_t workspace_bytes, pkv_stream_t stream, const int32_t* seq_prefix,
-                         int pre_slots) {
+                         int pre_slots, const FusedAppend* fused = nullptr) {
   if (!q || !block_tables || !context_lens || !out)
     return fail(PKV_ERR_INVALID_ARG, "q, block_tables, context_lens and out must be non-NULL");
   if (!aligned(q, 16)) return fail(PKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
@@ -538,6 +546,14 @@ pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32
     if (const char* env = std::getenv("PKV_CASCADE_DEFER")) defer = env[0] == '1';
     p.defer_prefix = defer ? 1 : 0;
   }
+  if (fused) {
+    p.fused = 1;
+    p.k_new = static_cast<const uint16_t*>(fused->k);
+    p.v_new = static_cast<const uint16_t*>(fused->v);
+    p.new_slots = fused->slots;
+    p.k_pool = cache->k_cache;
+    p.v_pool = cache->v_cache;
+  }
   // failure-detection tests: a short consumer wait and a late producer (tensor-core form)
   if (const char* env = std::getenv("PKV_TEST_CONSUMER_WAIT_CYCLES")) {
     const long long v = std::strtoll(env, nullptr, 10);
@@ -577,6 +593,33 @@ pkv_status pkv_paged_decode_attention(const pkv_cache_desc* cache, const void* q
   if (batch == 0) return PKV_OK;
   return decode_common(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, max_context_len,
                        softmax_scale, out, out_dtype, workspace, workspace_bytes, stream, nullptr, 0);
+}
+
+pkv_status pkv_paged_append_decode(const pkv_cache_desc* cache, const void* k, const void* v,
+                                   const int64_t* slot_mapping, const void* q, const int32_t* block_tables,
+                                   int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
+                                   int32_t num_q_heads, int32_t max_context_len, float softmax_scale, void* out,
+                                   pkv_out_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                                   pkv_stream_t stream) {
+  t_last_error.clear();
+  pkv_status st = check_cache(cache);
+  if (st != PKV_OK) return st;
+  if (batch < 0) return fail(PKV_ERR_INVALID_ARG, "batch must be >= 0");
+  if (batch == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping) return fail(PKV_ERR_INVALID_ARG, "k, v and slot_mapping must be non-NULL");
+  if (!aligned(k, 16) || !aligned(v, 16)) return fail(PKV_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  if (!aligned(slot_mapping, 8)) return fail(PKV_ERR_INVALID_ARG, "slot_mapping must be 8-byte aligned");
+  // The CUDA-core form has no fused append: the two calls, in order, compute the same.
+  if (!use_mma()) {
+    st = pkv_paged_kv_append(cache, k, v, slot_mapping, batch, stream);
+    if (st != PKV_OK) return st;
+    return pkv_paged_decode_attention(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads,
+                                      max_context_len, softmax_scale, out, out_dtype, workspace, workspace_bytes,
+                                      stream);
+  }
+  const FusedAppend fa{k, v, slot_mapping};
+  return decode_common(cache, q, block_tables, max_blocks_per_seq, context_lens, batch, num_q_heads, max_context_len,
+                       softmax_scale, out, out_dtype, workspace, workspace_bytes, stream, nullptr, 0, &fa);
 }
 
 pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void* q, const pkv_prefix_desc* px,

@@ -120,6 +120,25 @@ __device__ __forceinline__ float e4m3_x2m120(uint32_t w) {
   return __uint_as_float(static_cast<uint32_t>(sh) & 0x87f00000u);
 }
 
+// ------------------------------------------------------------------ E4M3 quantisation
+
+// Eight bf16 values (16 bytes) -> eight OCP E4M3 codes (8 bytes): each value divided by the
+// scale as an IEEE binary32 division, then rounded to nearest-even E4M3 with saturation to
+// +-448 (the append's encoding; the fused append of the decode uses the same function).
+__device__ __forceinline__ uint2 e4m3_quant8(uint4 w, float sc) {
+  const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+  uint32_t out[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float a0 = __fdiv_rn(bf16_lo(in[2 * j]), sc), a1 = __fdiv_rn(bf16_hi(in[2 * j]), sc);
+    const float a2 = __fdiv_rn(bf16_lo(in[2 * j + 1]), sc), a3 = __fdiv_rn(bf16_hi(in[2 * j + 1]), sc);
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a2, a3), __NV_SATFINITE, __NV_E4M3);
+    out[j] = (lo & 0xffffu) | (hi << 16);
+  }
+  return make_uint2(out[0], out[1]);
+}
+
 // ------------------------------------------------------------------ math
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
