@@ -50,4 +50,23 @@ PKV_DECLARE_PREFIX_TC(64, true)
 PKV_DECLARE_PREFIX_TC(128, true)
 #undef PKV_DECLARE_PREFIX_TC
 
+// The prefix pass for small member groups of an E4M3 pool on mma.sync
+// (cascade_prefix_mma.cu): at most 16 MT query rows per (prefix, kv head), grid.x = 1; the
+// pools are read through tensor maps of 16 rows x D codes with the 128-byte (D = 128) or
+// 64-byte (D = 64) swizzle.
+template <int D, int MT>
+int cascade_prefix_mma_ctas_per_sm(int device);  // CTAs of the pass resident per SM; 0 on error
+template <int D, int MT>
+cudaError_t launch_cascade_prefix_mma(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p, dim3 grid,
+                                      cudaStream_t stream, int device);
+#define PKV_DECLARE_PREFIX_MMA(D, MT)                                                                        \
+  extern template int cascade_prefix_mma_ctas_per_sm<D, MT>(int);                                           \
+  extern template cudaError_t launch_cascade_prefix_mma<D, MT>(const CUtensorMap&, const CUtensorMap&,      \
+                                                               const PrefixParams&, dim3, cudaStream_t, int);
+PKV_DECLARE_PREFIX_MMA(64, 1)
+PKV_DECLARE_PREFIX_MMA(64, 2)
+PKV_DECLARE_PREFIX_MMA(128, 1)
+PKV_DECLARE_PREFIX_MMA(128, 2)
+#undef PKV_DECLARE_PREFIX_MMA
+
 }  // namespace pkv

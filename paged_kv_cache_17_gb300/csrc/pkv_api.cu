@@ -203,6 +203,22 @@ bool encode_kv_map_sw128(CUtensorMap* tm, void* base, int64_t num_blocks, int hk
   return r == CUDA_SUCCESS;
 }
 
+// The pool's E4M3 codes as boxes of 16 rows x D codes, swizzled so that the mma.sync prefix
+// pass reads its per-lane runs of codes without bank conflicts: the 128-byte swizzle for
+// 128-byte rows (D = 128), the 64-byte swizzle for 64-byte rows (D = 64).
+bool encode_kv_map_e4m3_swz(CUtensorMap* tm, void* base, int64_t num_blocks, int hkv, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                              static_cast<cuuint64_t>(num_blocks) * 16};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv) * d};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Splits of the prefix pass: each split is a run of whole 64-key stages (a multiple of four
 // blocks), at least two stages long, at most kMaxPrefixRecords per prefix; the count
 // minimises (waves of CTAs, `slots` = SMs x CTAs resident per SM at a time) x (blocks per
@@ -420,12 +436,23 @@ size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
   // the most prefix records either pool type plans for (its CTAs per SM set the splits)
   int device = 0;
   cudaGetDevice(&device);
-  const int per_sm[2] = {head_dim == 64 ? pkv::cascade_prefix_tc_ctas_per_sm<64, false>(device)
+  // (the tcgen05 pass for either pool type, and the mma.sync pass for small E4M3 groups)
+  const bool small = static_cast<long long>(max_members) * (num_q_heads / num_kv_heads) <= 32;
+  const bool mt1 = static_cast<long long>(max_members) * (num_q_heads / num_kv_heads) <= 16;
+  int per_sm[4] = {head_dim == 64 ? pkv::cascade_prefix_tc_ctas_per_sm<64, false>(device)
                                         : pkv::cascade_prefix_tc_ctas_per_sm<128, false>(device),
                          head_dim == 64 ? pkv::cascade_prefix_tc_ctas_per_sm<64, true>(device)
-                                        : pkv::cascade_prefix_tc_ctas_per_sm<128, true>(device)};
+                                        : pkv::cascade_prefix_tc_ctas_per_sm<128, true>(device),
+                         !small ? 1
+                         : head_dim == 64
+                             ? (mt1 ? pkv::cascade_prefix_mma_ctas_per_sm<64, 1>(device)
+                                    : pkv::cascade_prefix_mma_ctas_per_sm<64, 2>(device))
+                             : (mt1 ? pkv::cascade_prefix_mma_ctas_per_sm<128, 1>(device)
+                                    : pkv::cascade_prefix_mma_ctas_per_sm<128, 2>(device)),
+                         1};
+  per_sm[3] = std::min(per_sm[2], 2);  // the mma.sync pass as the cascade call plans it
   PrefixPlan pp{0, 0, 0};
-  for (int k = 0; k < 2; ++k) {
+  for (int k = 0; k < 4; ++k) {
     if (per_sm[k] <= 0) {
       fail(PKV_ERR_CUDA, "the prefix pass does not fit on an SM of this device");
       return 0;
@@ -658,7 +685,23 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   const bool fp8 = cache->kv_dtype == PKV_KV_FP8_E4M3;
   int device = 0;
   cudaGetDevice(&device);
-  const int per_sm = cache->head_dim == 64
+  // Small member groups of an E4M3 pool (at most 32 query rows per prefix and kv head, such
+  // as a best-of-8 fork with G = 4) take the mma.sync pass, which reads the codes straight
+  // into its MMA fragments; the rest the tcgen05 pass with its 128-row tiles.
+  // PKV_PREFIX_PASS=tc | mma picks one where both apply (tuning and tests).
+  const long long group_rows = static_cast<long long>(px->max_members) * g;
+  bool mma_pass = fp8 && group_rows <= 32;
+  if (const char* env = std::getenv("PKV_PREFIX_PASS")) {
+    if (std::strcmp(env, "tc") == 0) mma_pass = false;
+    else if (std::strcmp(env, "mma") == 0) mma_pass = fp8 && group_rows <= 32;
+  }
+  const int mma_mt = group_rows <= 16 ? 1 : 2;
+  const int per_sm = mma_pass ? (cache->head_dim == 64
+                                     ? (mma_mt == 1 ? pkv::cascade_prefix_mma_ctas_per_sm<64, 1>(device)
+                                                    : pkv::cascade_prefix_mma_ctas_per_sm<64, 2>(device))
+                                     : (mma_mt == 1 ? pkv::cascade_prefix_mma_ctas_per_sm<128, 1>(device)
+                                                    : pkv::cascade_prefix_mma_ctas_per_sm<128, 2>(device)))
+                   : cache->head_dim == 64
                          ? (fp8 ? pkv::cascade_prefix_tc_ctas_per_sm<64, true>(device)
                                 : pkv::cascade_prefix_tc_ctas_per_sm<64, false>(device))
                          : (fp8 ? pkv::cascade_prefix_tc_ctas_per_sm<128, true>(device)
@@ -668,13 +711,16 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   // stream the sequences' own blocks while the prefix pass runs (shared-prefix step 82.7 ->
   // 75.4 us); E4M3 pools: every CTA an SM holds (the prefix pass is the longer part there,
   // fork step 64.4 -> 56.3 us).  PKV_PREFIX_CTAS_PER_SM overrides this, for tuning and tests.
-  int plan_per_sm = fp8 ? per_sm : 1;
+  // The mma.sync pass (four per SM fit): two per SM, so that decode CTAs stream the sequences'
+  // own blocks beside it (fork step 55.7 -> 53.8 us).
+  int plan_per_sm = mma_pass ? std::min(per_sm, 2) : (fp8 ? per_sm : 1);
   if (const char* env = std::getenv("PKV_PREFIX_CTAS_PER_SM")) {
     const long v = std::strtol(env, nullptr, 10);
     if (v >= 1 && v <= per_sm) plan_per_sm = static_cast<int>(v);
   }
-  const PrefixPlan pp = plan_prefix(px->num_prefixes, px->max_members, px->max_prefix_len, g, hkv,
-                                    static_cast<long long>(dev->sm_count) * plan_per_sm);
+  PrefixPlan pp = plan_prefix(px->num_prefixes, px->max_members, px->max_prefix_len, g, hkv,
+                              static_cast<long long>(dev->sm_count) * plan_per_sm);
+  if (mma_pass) pp.tiles = 1;
   if (static_cast<long long>(px->num_prefixes) * pp.pre_slots > 65535 || pp.tiles > 0x7fffffff / 2)
     return fail(PKV_ERR_UNSUPPORTED, "too many prefixes for the prefix-pass grid");
   Split sp;
@@ -692,10 +738,12 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
 
   CUtensorMap tk, tv;
   const bool maps_ok =
-      fp8 ? encode_kv_map(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim, true) &&
-                encode_kv_map(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim, true)
-          : encode_kv_map_sw128(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim) &&
-                encode_kv_map_sw128(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim);
+      mma_pass ? encode_kv_map_e4m3_swz(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim) &&
+                     encode_kv_map_e4m3_swz(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim)
+      : fp8 ? encode_kv_map(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim, true) &&
+                  encode_kv_map(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim, true)
+            : encode_kv_map_sw128(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim) &&
+                  encode_kv_map_sw128(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim);
   if (!maps_ok) return fail(PKV_ERR_INVALID_ARG, "cannot describe the KV pool as a TMA tensor map");
   pkv::PrefixParams pr{};
   pr.q = static_cast<const uint16_t*>(q);
@@ -723,7 +771,14 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
                    static_cast<unsigned>(px->num_prefixes * pp.pre_slots));
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
-  if (cache->head_dim == 64)
+  if (mma_pass) {
+    if (cache->head_dim == 64)
+      e = mma_mt == 1 ? pkv::launch_cascade_prefix_mma<64, 1>(tk, tv, pr, pgrid, cs, device)
+                      : pkv::launch_cascade_prefix_mma<64, 2>(tk, tv, pr, pgrid, cs, device);
+    else
+      e = mma_mt == 1 ? pkv::launch_cascade_prefix_mma<128, 1>(tk, tv, pr, pgrid, cs, device)
+                      : pkv::launch_cascade_prefix_mma<128, 2>(tk, tv, pr, pgrid, cs, device);
+  } else if (cache->head_dim == 64)
     e = fp8 ? pkv::launch_cascade_prefix_tc<64, true>(tk, tv, pr, pgrid, cs, device)
             : pkv::launch_cascade_prefix_tc<64, false>(tk, tv, pr, pgrid, cs, device);
   else
