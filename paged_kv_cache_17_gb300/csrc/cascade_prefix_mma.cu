@@ -79,21 +79,6 @@ struct MmaPrefixCfg {
 
 namespace {
 
-// byte offset of 16-byte chunk c of row r in a tile of 16 rows x D codes, as the swizzled
-// TMA load writes it (128-byte swizzle for 128-byte rows, 64-byte swizzle for 64-byte rows)
-template <int D>
-__device__ __forceinline__ int code_off(int r, int c) {
-  if constexpr (D == 128) return r * 128 + ((c ^ (r & 7)) << 4);
-  else return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
-}
-
-__device__ __forceinline__ uint32_t cvt_lo(uint32_t w) { return e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xffffu)); }
-__device__ __forceinline__ uint32_t cvt_hi(uint32_t w) { return e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)); }
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
-}
-
 // 2^x by the hardware approximation with subnormal inputs and results flushed to zero
 __device__ __forceinline__ float exp2_ftz(float x) {
   float y;
@@ -296,7 +281,7 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int c = 0; c < KCH; ++c)
-        kr[nt][c] = *reinterpret_cast<const uint4*>(kt + code_off<D>(8 * nt + gid, tig * KCH + c));
+        kr[nt][c] = *reinterpret_cast<const uint4*>(kt + e4m3_off<D>(8 * nt + gid, tig * KCH + c));
     // ---- scores, two independent accumulation chains per n-tile
     float acc[2][2][4];
 #pragma unroll
@@ -308,8 +293,8 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
       const uint4 a = qw[kk * 32];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const uint32_t w = word_of(kr[nt][kk / 4], kk % 4);
-        mma16<true>(acc[nt][kk & 1], a.x, a.y, a.z, a.w, cvt_lo(w), cvt_hi(w));
+        const uint32_t w = u4_word(kr[nt][kk / 4], kk % 4);
+        mma16<true>(acc[nt][kk & 1], a.x, a.y, a.z, a.w, e4m3_lo(w), e4m3_hi(w));
       }
     }
     float s[2][4];
@@ -324,13 +309,13 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
     for (int t = 0; t < 4; ++t) {
       const int tok = 2 * tig + (t & 1) + 8 * (t >> 1);  // V codes gid * D/8 .. + D/8
       if constexpr (D == 128) {
-        const uint4 v = *reinterpret_cast<const uint4*>(vt + code_off<D>(tok, gid));
+        const uint4 v = *reinterpret_cast<const uint4*>(vt + e4m3_off<D>(tok, gid));
         vr[t][0] = v.x;
         vr[t][1] = v.y;
         vr[t][2] = v.z;
         vr[t][3] = v.w;
       } else {
-        const uint2 v = *reinterpret_cast<const uint2*>(vt + code_off<D>(tok, gid >> 1) + (gid & 1) * 8);
+        const uint2 v = *reinterpret_cast<const uint2*>(vt + e4m3_off<D>(tok, gid >> 1) + (gid & 1) * 8);
         vr[t][0] = v.x;
         vr[t][1] = v.y;
       }
@@ -393,10 +378,10 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
     for (int i = 0; i < NT / 4; ++i) {
       const uint32_t x01 = __byte_perm(vr[0][i], vr[1][i], 0x5140), y01 = __byte_perm(vr[0][i], vr[1][i], 0x7362);
       const uint32_t x89 = __byte_perm(vr[2][i], vr[3][i], 0x5140), y89 = __byte_perm(vr[2][i], vr[3][i], 0x7362);
-      mma16<true>(o[4 * i + 0], pa0, pa1, pa2, pa3, cvt_lo(x01), cvt_lo(x89));
-      mma16<true>(o[4 * i + 1], pa0, pa1, pa2, pa3, cvt_hi(x01), cvt_hi(x89));
-      mma16<true>(o[4 * i + 2], pa0, pa1, pa2, pa3, cvt_lo(y01), cvt_lo(y89));
-      mma16<true>(o[4 * i + 3], pa0, pa1, pa2, pa3, cvt_hi(y01), cvt_hi(y89));
+      mma16<true>(o[4 * i + 0], pa0, pa1, pa2, pa3, e4m3_lo(x01), e4m3_lo(x89));
+      mma16<true>(o[4 * i + 1], pa0, pa1, pa2, pa3, e4m3_hi(x01), e4m3_hi(x89));
+      mma16<true>(o[4 * i + 2], pa0, pa1, pa2, pa3, e4m3_lo(y01), e4m3_lo(y89));
+      mma16<true>(o[4 * i + 3], pa0, pa1, pa2, pa3, e4m3_hi(y01), e4m3_hi(y89));
     }
   }
   // every copy the loader issued lands before the ring is reused as scratch (on the normal

@@ -62,10 +62,9 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
 
 // The tensor-core form: same grid and launch, a 32 KiB ring of K and V tiles.  bf16 pools:
 // 2 consumer warps and 128-byte-swizzled boxes (4 stages at D = 128; six CTAs per SM); E4M3
-// pools: 4 consumer warps, each expanding its own tiles into 8 KiB of fp16 (the expansion
-// is CUDA-core work that wants the extra warps; three CTAs per SM).  Measured against 4/8,
-// 2/6, 1/2 and 1/4 (warps/stages) on the 8B-shaped, 70B-shaped, short-suffix and fork
-// steps.
+// pools: 4 consumer warps (the expansion of the codes is CUDA-core work that wants the
+// extra warps), 8 stages at D = 128.  Measured against 4/8, 2/6, 1/2 and 1/4 (warps/stages)
+// on the 8B-shaped, 70B-shaped, short-suffix and fork steps.
 template <int D, bool FP8>
 struct MmaShape {
   static constexpr int kNWC = FP8 ? 4 : 2;

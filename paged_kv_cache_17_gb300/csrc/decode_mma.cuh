@@ -19,11 +19,17 @@
 // ldmatrix (V transposed); q stays in registers as B fragments; the weights P leave the S
 // accumulators through movmatrix (an 8x8 transpose inside the warp) as the B operand of
 // the second product, split into bf16 hi + lo so that P V keeps fp32-level accuracy.
-// E4M3 pools: the raw codes arrive in the ring; the consuming warp expands its tile exactly
-// to fp16 (cvt.rn.f16x2.e4m3x2) into a private swizzled tile, releases the ring slot, and
-// runs the products in fp16 -- q scaled per head by a power of two into fp16's range (the
-// factor is folded into that head's score scale), the K scale into the score scale, the V
-// scale into the output.
+// E4M3 pools: the raw codes arrive in the ring (128-byte swizzle at D = 128, 64-byte at
+// D = 64) and go straight into the MMA fragments, expanded exactly to fp16 in registers
+// (cvt.rn.f16x2.e4m3x2), with no expanded copy in shared memory.  The score product
+// contracts over the head dimension, so any permutation applied to K and q alike leaves it
+// unchanged: lane (gid, tig) takes dims tig*D/4 .. +D/4 of every k-step's pairs, and its K
+// operand is D/4 consecutive codes of tokens gid and gid + 8 (16-byte loads).  In the
+// output product, row r of m-tile mt is dim (r mod 8)*D/8 + 2 mt + r/8, so a lane's V
+// operand is D/8 consecutive codes of each of its four tokens, paired by byte permutes
+// before the expansion; the output rows come back with the same map.  The products run in
+// fp16 -- q scaled per head by a power of two into fp16's range (the factor is folded into
+// that head's score scale), the K scale into the score scale, the V scale into the output.
 #pragma once
 
 #include "decode_kernel.cuh"
@@ -40,9 +46,8 @@ struct MmaCfg {
   static constexpr int kMT = D / 16;                      // m-tiles of the output product
   static constexpr int kThreads = (NWC + 1) * 32;
   static constexpr int kRingBytes = 2 * STAGES * kRingTile;
-  static constexpr int kConvBytes = FP8 ? NWC * 2 * kTileBytes : 0;  // per warp: expanded K, V
   static constexpr int kTilesBytes = kRingBytes;
-  static constexpr int kBarOffset = kRingBytes + kConvBytes;
+  static constexpr int kBarOffset = kRingBytes;
   static constexpr int kSmemBytes = 1024 + kBarOffset + 2 * STAGES * 8;  // 1024: alignment slack
   // merge scratch: the warps' states, then (cascade) the prefix records' (m, l) pairs and
   // the weights of every part
@@ -176,8 +181,13 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
     const uint32_t* qr = reinterpret_cast<const uint32_t*>(p.q + (static_cast<size_t>(b) * p.hq + hq0 + (live ? gid : 0)) * D);
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) {
-      qb[kk][0] = live ? qr[kk * 8 + tig] : 0u;      // dims 16kk + 2tig, +1
-      qb[kk][1] = live ? qr[kk * 8 + 4 + tig] : 0u;  // dims 16kk + 8 + 2tig, +1
+      if constexpr (FP8) {  // the permuted order: dims tig*D/4 + 4kk + {0, 1} | {2, 3}
+        qb[kk][0] = live ? qr[tig * (D / 8) + 2 * kk] : 0u;
+        qb[kk][1] = live ? qr[tig * (D / 8) + 2 * kk + 1] : 0u;
+      } else {
+        qb[kk][0] = live ? qr[kk * 8 + tig] : 0u;      // dims 16kk + 2tig, +1
+        qb[kk][1] = live ? qr[kk * 8 + 4 + tig] : 0u;  // dims 16kk + 8 + 2tig, +1
+      }
     }
     if constexpr (FP8) {
       // the head's largest |q| (over the 4 lanes of equal gid) goes to 2^13 .. 2^14
@@ -292,8 +302,9 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         if (lane < 2 * kRowChunks) {
           const bool isv = lane >= kRowChunks;
           const int c = lane % kRowChunks;
-          if constexpr (FP8) {  // the raw codes, before this warp expands them
-            uint8_t* rowp = (isv ? v_tiles : k_tiles) + sg * C::kRingTile + (valid - 1) * D + c * 8;
+          if constexpr (FP8) {  // the raw codes (8 of them: half of a swizzled 16-byte chunk)
+            uint8_t* rowp =
+                (isv ? v_tiles : k_tiles) + sg * C::kRingTile + e4m3_off<D>(valid - 1, c >> 1) + (c & 1) * 8;
             *reinterpret_cast<uint2*>(rowp) = make_uint2(newrow.x, newrow.y);
           } else {
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz_addr<D>(isv ? vb : kb, valid - 1, c)),
@@ -303,42 +314,52 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         }
         __syncwarp();
       }
-      if constexpr (FP8) {
-        // expand both tiles into this warp's fp16 tiles: 8 codes -> one swizzled 16-byte chunk
-        const uint32_t kc = smem_u32(smem + C::kRingBytes + warp * 2 * C::kTileBytes);
-        const uint32_t vc = kc + C::kTileBytes;
-        const uint8_t* rk = k_tiles + sg * C::kRingTile;
-        const uint8_t* rv = v_tiles + sg * C::kRingTile;
-        constexpr int kChunks = kBlockSize * (D / 8);
-#pragma unroll
-        for (int i = 0; i < 2 * kChunks / 32; ++i) {
-          const int ci = lane + 32 * i;
-          const bool isv = ci >= kChunks;
-          const int cj = isv ? ci - kChunks : ci;
-          const int r = cj / (D / 8), c = cj % (D / 8);
-          const uint2 raw = *reinterpret_cast<const uint2*>((isv ? rv : rk) + r * D + c * 8);
-          const uint32_t h0 = e4m3x2_to_f16x2(static_cast<uint16_t>(raw.x & 0xffffu));
-          const uint32_t h1 = e4m3x2_to_f16x2(static_cast<uint16_t>(raw.x >> 16));
-          const uint32_t h2 = e4m3x2_to_f16x2(static_cast<uint16_t>(raw.y & 0xffffu));
-          const uint32_t h3 = e4m3x2_to_f16x2(static_cast<uint16_t>(raw.y >> 16));
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(swz_addr<D>(isv ? vc : kc, r, c)), "r"(h0),
-                       "r"(h1), "r"(h2), "r"(h3)
-                       : "memory");
-        }
-        fence_proxy_async_smem();  // the codes were read through the generic proxy; TMA refills the slot
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[sg]);  // the ring slot is free again
-        kb = kc;
-        vb = vc;
-      }
-
       // ---- S^T = K q^T: rows = tokens gid, gid+8; columns = heads 2tig, 2tig+1
       float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t vr[4][D / 32];  // E4M3: V codes gid*D/8 .. +D/8 of tokens 2tig, 2tig+1, 2tig+8, 2tig+9
+      if constexpr (FP8) {
+        // K codes tig*D/4 .. +D/4 of tokens gid and gid + 8, each word one k-step's pairs
+        constexpr int KCH = D / 64;  // 16-byte chunks per token and lane
+        uint4 kr[2][KCH];
+        const uint8_t* kt = k_tiles + sg * C::kRingTile;
+        const uint8_t* vt = v_tiles + sg * C::kRingTile;
 #pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(swz_addr<D>(kb, (lane & 7) + 8 * (mi & 1), 2 * kk + (mi >> 1)), a0, a1, a2, a3);
-        mma16<FP8>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int c = 0; c < KCH; ++c)
+            kr[r][c] = *reinterpret_cast<const uint4*>(kt + e4m3_off<D>(gid + 8 * r, tig * KCH + c));
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint32_t w0 = u4_word(kr[0][kk / 4], kk % 4), w1 = u4_word(kr[1][kk / 4], kk % 4);
+          mma16<FP8>(sc, e4m3_lo(w0), e4m3_lo(w1), e4m3_hi(w0), e4m3_hi(w1), qb[kk][0], qb[kk][1]);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int tok = 2 * tig + (t & 1) + 8 * (t >> 1);
+          if constexpr (D == 128) {
+            const uint4 v = *reinterpret_cast<const uint4*>(vt + e4m3_off<D>(tok, gid));
+            vr[t][0] = v.x;
+            vr[t][1] = v.y;
+            vr[t][2] = v.z;
+            vr[t][3] = v.w;
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(vt + e4m3_off<D>(tok, gid >> 1) + (gid & 1) * 8);
+            vr[t][0] = v.x;
+            vr[t][1] = v.y;
+          }
+        }
+        // both tiles are in registers: the ring slot goes back (the reads went through the
+        // generic proxy, the refill comes through the async proxy)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[sg]);
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(swz_addr<D>(kb, (lane & 7) + 8 * (mi & 1), 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+          mma16<FP8>(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -378,20 +399,40 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
       split16<FP8>(p2, p3, h23, l23);  // token gid + 8
       const uint32_t bh0 = movm_t(h01), bh1 = movm_t(h23);  // head gid: tokens 2tig.., 8 + 2tig..
       const uint32_t bl0 = movm_t(l01), bl1 = movm_t(l23);
-      // ---- O^T += V^T P^T: m-tile mt = dims 16mt .. 16mt + 15
+      if constexpr (FP8) {
+        // ---- O^T += V^T P^T: code word i of each token holds dims gid*D/8 + 4i .. + 3, the
+        // rows gid and gid + 8 of m-tiles 2i and 2i + 1; a byte permute pairs tokens
+        // (2tig, 2tig+1) and (2tig+8, 2tig+9)
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(swz_addr<D>(vb, (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a0, a1, a2, a3);
-        mma16<FP8>(o[mt], a0, a1, a2, a3, bh0, bh1);
-        mma16<FP8>(o[mt], a0, a1, a2, a3, bl0, bl1);
+        for (int i = 0; i < D / 32; ++i) {
+          const uint32_t x01 = __byte_perm(vr[0][i], vr[1][i], 0x5140), y01 = __byte_perm(vr[0][i], vr[1][i], 0x7362);
+          const uint32_t x89 = __byte_perm(vr[2][i], vr[3][i], 0x5140), y89 = __byte_perm(vr[2][i], vr[3][i], 0x7362);
+          const uint32_t e0 = e4m3_lo(x01), e1 = e4m3_hi(x01), e2 = e4m3_lo(x89), e3 = e4m3_hi(x89);
+          mma16<FP8>(o[2 * i], e0, e1, e2, e3, bh0, bh1);
+          mma16<FP8>(o[2 * i], e0, e1, e2, e3, bl0, bl1);
+          const uint32_t f0 = e4m3_lo(y01), f1 = e4m3_hi(y01), f2 = e4m3_lo(y89), f3 = e4m3_hi(y89);
+          mma16<FP8>(o[2 * i + 1], f0, f1, f2, f3, bh0, bh1);
+          mma16<FP8>(o[2 * i + 1], f0, f1, f2, f3, bl0, bl1);
+        }
+      } else {
+        // ---- O^T += V^T P^T: m-tile mt = dims 16mt .. 16mt + 15
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(swz_addr<D>(vb, (lane & 7) + 8 * (mi >> 1), 2 * mt + (mi & 1)), a0, a1, a2, a3);
+          mma16<FP8>(o[mt], a0, a1, a2, a3, bh0, bh1);
+          mma16<FP8>(o[mt], a0, a1, a2, a3, bl0, bl1);
+        }
       }
       // The ring tiles were read with ldmatrix (generic proxy) and the producer refills them
       // with TMA (async proxy): without this fence the refill can land while a read of the
-      // stage is still pending (seen as wrong output dims in repeated runs).
-      if constexpr (!FP8) fence_proxy_async_smem();
-      __syncwarp();  // the tiles are read (E4M3: this warp's fp16 tiles are rewritten next)
-      if (!FP8 && lane == 0) mbar_arrive(&empty_bar[sg]);
+      // stage is still pending (seen as wrong output dims in repeated runs).  (E4M3: the
+      // slot went back right after the loads.)
+      if constexpr (!FP8) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[sg]);
+      }
     }
   }
 
@@ -414,8 +455,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32)
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-          aw[(warp * G + g) * D + 16 * mt + gid] = o[mt][j];
-          aw[(warp * G + g) * D + 16 * mt + gid + 8] = o[mt][2 + j];
+          // rows gid and gid + 8 of m-tile mt: dims 16mt + gid and + 8 (E4M3: gid*D/8 + 2mt, + 1)
+          const int d0 = FP8 ? gid * (D / 8) + 2 * mt : 16 * mt + gid;
+          const int d1 = FP8 ? d0 + 1 : d0 + 8;
+          aw[(warp * G + g) * D + d0] = o[mt][j];
+          aw[(warp * G + g) * D + d1] = o[mt][2 + j];
         }
       }
     }

@@ -95,6 +95,26 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t codes) {
   return r;
 }
 
+// Byte offset of 16-byte chunk c of row r in a tile of 16 rows x D one-byte (E4M3) codes, as
+// the swizzled TMA load writes it: the 128-byte swizzle for 128-byte rows (D = 128: the chunk
+// index xor-ed with r mod 8), the 64-byte swizzle for 64-byte rows (D = 64: xor-ed with
+// (r / 2) mod 4).  Under it, 16-byte loads of one chunk per row from 8 consecutive rows, or
+// of 8 chunks of one row, meet no bank conflicts.
+template <int D>
+__device__ __forceinline__ int e4m3_off(int r, int c) {
+  static_assert(D == 64 || D == 128, "head_dim");
+  if constexpr (D == 128) return r * 128 + ((c ^ (r & 7)) << 4);
+  else return r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
+// codes 0, 1 (e4m3_lo) or 2, 3 (e4m3_hi) of a 32-bit word of four E4M3 codes as an fp16 pair
+__device__ __forceinline__ uint32_t e4m3_lo(uint32_t w) { return e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xffffu)); }
+__device__ __forceinline__ uint32_t e4m3_hi(uint32_t w) { return e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16)); }
+
+__device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
 // Shared address of row r (0..15 within a 16-row box group) and 16-byte chunk c of a tile
 // stored as boxes of 16 rows x 128 bytes (64 16-bit elements), one box per 64 columns,
 // 128-byte swizzled: the chunk index within a row is xor-ed with the row index mod 8.

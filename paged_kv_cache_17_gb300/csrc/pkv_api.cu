@@ -531,14 +531,18 @@ pkv_status decode_common(const pkv_cache_desc* cache, const void* q, const int32
     if (workspace_bytes < ws.total)
       return fail(PKV_ERR_WORKSPACE, "workspace has %zu bytes, %zu required", workspace_bytes, ws.total);
   }
+  // the tensor-core form reads swizzled boxes (bf16: 64-column halves; E4M3: whole rows of
+  // codes), the CUDA-core form plain ones
   CUtensorMap tk, tv;
   const bool maps_ok =
       var.swizzled ? encode_kv_map_sw128(&tk, cache->k_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim) &&
                          encode_kv_map_sw128(&tv, cache->v_cache, cache->num_blocks, cache->num_kv_heads,
                                              cache->head_dim)
-                   : encode_kv_map(&tk, cache->k_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8) &&
-                         encode_kv_map(&tv, cache->v_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim,
-                                       fp8);
+      : (fp8 && var.tensor_core)
+          ? encode_kv_map_e4m3_swz(&tk, cache->k_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim) &&
+                encode_kv_map_e4m3_swz(&tv, cache->v_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim)
+          : encode_kv_map(&tk, cache->k_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8) &&
+                encode_kv_map(&tv, cache->v_cache, cache->num_blocks, cache->num_kv_heads, cache->head_dim, fp8);
   if (!maps_ok) return fail(PKV_ERR_INVALID_ARG, "cannot describe the KV pool as a TMA tensor map");
 
   pkv::DecodeParams p{};
