@@ -60,14 +60,14 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
   return cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
 }
 
-// The tensor-core form: same grid and launch, a 32 KiB ring of K and V tiles.  bf16 pools:
-// 2 consumer warps and 128-byte-swizzled boxes (4 stages at D = 128; six CTAs per SM); E4M3
-// pools: 4 consumer warps (the expansion of the codes is CUDA-core work that wants the
-// extra warps), 8 stages at D = 128.  Measured against 4/8, 2/6, 1/2 and 1/4 (warps/stages)
-// on the 8B-shaped, 70B-shaped, short-suffix and fork steps.
+// The tensor-core form: same grid and launch, 2 consumer warps and a 32 KiB ring of K and V
+// tiles (bf16: 4 stages at D = 128; E4M3: 8), six CTAs per SM (shared-memory limit).  bf16
+// measured against 4/8, 2/6, 1/2 and 1/4 (warps/stages) on the 8B-shaped, 70B-shaped and
+// short-suffix steps; E4M3 against 4 warps (fork decode 127.0 against 94.2 us), 1 warp,
+// and 16 or 64 KiB rings.
 template <int D, bool FP8>
 struct MmaShape {
-  static constexpr int kNWC = FP8 ? 4 : 2;
+  static constexpr int kNWC = 2;
   static constexpr int kRingTile = FP8 ? 16 * D : 16 * D * 2;
   static constexpr int kStages = 32768 / (2 * kRingTile);
 };
