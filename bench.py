@@ -106,13 +106,22 @@ def step_bytes(w: W.Workload) -> dict:
             "logical_kv": w.logical_kv_bytes()}
 
 
-def decode_kernel_name(cfg, cascade: bool) -> str:
+def decode_kernel_name(cfg, cascade: bool, w=None) -> str:
     """The kernels inside the decode call's timed interval (the merge runs for split
-    sequences, and for cascades, whose prefix records it merges)."""
+    sequences, and for cascades, whose prefix records it merges).  A cascade's prefix pass
+    runs on mma.sync for groups of at most 32 query rows over an E4M3 pool, else on tcgen05."""
     tc = os.environ.get("PKV_DECODE_CUDA_CORES") != "1"  # both pool types run the tensor-core form
     core = "paged_decode_mma_kernel (tensor cores)" if tc else "paged_decode_kernel (CUDA cores)"
     name = core + " + merge_partitions_kernel"
-    return ("cascade_prefix_tc_kernel (tcgen05) + " + name) if cascade else name
+    if not cascade:
+        return name
+    small = False
+    if w is not None and w.scales is not None:
+        c = w.cascade()
+        small = c.max_members * (cfg.hq // cfg.hkv) <= 32
+    if not small or os.environ.get("PKV_PREFIX_PASS") == "tc":
+        return "cascade_prefix_tc_kernel (tcgen05) + " + name
+    return "cascade_prefix_mma_kernel (mma.sync) + " + name
 
 
 def measured_peaks() -> dict:
@@ -408,6 +417,7 @@ def summary_entry(tm: Timed, step_ms, dec_ms, read_ms, peak: float, ws: int, dev
     achieved = nb["decode"] / (dec_avg * 1e-3) / 1e9
     e = {"decode_call": "cascade" if tm.cas is not None else "paged", "batch": B,
          "total_context_tokens": tm.w.total_tokens(), "unique_kv_bytes": nb["unique_kv"],
+         "kernel": decode_kernel_name(tm.cfg, tm.cas is not None, tm.w),
          "decode_bytes": nb["decode"], "step_us": round(step_tot / n * 1e3, 2), "decode_us": round(dec_avg * 1e3, 2),
          "decode_us_p10_p50_p90": [round(float(x) * 1e3, 2) for x in np.percentile(dec_ms, [10, 50, 90])],
          "unique_kv_gbs": round(nb["unique_kv"] / (dec_avg * 1e-3) / 1e9, 1),
@@ -614,7 +624,7 @@ def run_ours(args):
         "decode_seq_steps_per_s": head["decode_seq_steps_per_s"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None if cas is not None else ncu_traffic(cfg.name),
-                     "kernel": decode_kernel_name(cfg, cas is not None),
+                     "kernel": decode_kernel_name(cfg, cas is not None, w),
                      "peak_source": f"{peak_src} hbm_gbs (copy)",
                      "frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4)},
         "read_ceiling": head.get("read_ceiling"),
