@@ -4,8 +4,10 @@ most 32 query rows per prefix and kv head -- on shapes beyond the fork workload:
 split longer than the 32 KiB load ring and many short splits, prefixes of different lengths
 (the shorter ones get empty splits), members whose whole context is the prefix, scores that
 grow along the prefix (rows move their reference max and the output is rescaled), the
-tcgen05 pass on the same inputs, and repeated calls.  PKV_PREFIX_SPLIT_BLOCKS fixes the
-blocks per split.
+tcgen05 pass on the same inputs, repeated calls, and block ids outside the pool (read as
+zeros and flagged, by both prefix passes and by the E4M3 decode, whose codes also go straight
+from the swizzled tiles into the MMA fragments).  PKV_PREFIX_SPLIT_BLOCKS fixes the blocks
+per split.
 
 Reference: the oracle's plain decode over each sequence's whole table -- attention over the
 prefix keys and over the own keys combine exactly (habr.com/ru/articles/1021832, section 3,
@@ -132,3 +134,70 @@ def test_repeated_calls_give_identical_bits(pkv):
     with env(PKV_PREFIX_PASS="mma", PKV_PREFIX_SPLIT_BLOCKS=12):
         outs = [run(pkv, c, kd, vd, q, 128 ** -0.5, scales=scales) for _ in range(10)]
     assert all((o == outs[0]).all() for o in outs[1:]), "repeated calls differ"
+
+
+def _zero_block_reference(case, d, bad_rows):
+    """The oracle's answer when the prefix table entries in `bad_rows` ((prefix, block index)
+    pairs) point outside the pool: such a block reads as zeros (K and V), so every sequence
+    of that prefix sees a zero block in that place."""
+    c, k8, v8, scales, q, full, lens = case
+    nb = k8.shape[0]
+    kz = torch.cat([k8, torch.zeros_like(k8[:1])])  # block nb: all-zero codes
+    vz = torch.cat([v8, torch.zeros_like(v8[:1])])
+    full = full.clone()
+    for pfx, j in bad_rows:
+        members = c.member_seqs[c.member_indptr[pfx]:c.member_indptr[pfx + 1]].tolist()
+        for b in members:
+            full[b, j] = nb
+    return oracle.decode_all(W.bf16_bits(q), kz.numpy(), vz.numpy(), oracle.KV_E4M3, full.numpy(), lens.numpy(),
+                             d ** -0.5, scales=scales.numpy())
+
+
+@pytest.mark.parametrize("kind", ["mma", "tc"])
+def test_out_of_pool_prefix_block_reads_zeros_and_is_flagged(pkv, kind):
+    """A prefix table entry past the pool (and a negative one) is read as a block of zeros by
+    either prefix pass and flagged in the device status; nothing else changes."""
+    case = build_groups(2, 4, 128, [(8, 30), (5, 20)], seed=2500)
+    c = case[0]
+    nb = case[1].shape[0]
+    c.prefix_tables[0, 3] = nb
+    c.prefix_tables[1, 7] = -1
+    d = 128
+    with env(PKV_PREFIX_PASS=kind, PKV_PREFIX_SPLIT_BLOCKS=8):
+        out = torch.empty(case[4].shape, dtype=torch.float32, device="cuda")
+        pkv.cascade_decode_attention(case[4].cuda(), case[1].cuda(), case[2].cuda(), c.prefix_tables.cuda(),
+                                     c.prefix_lens.cuda(), c.member_indptr.cuda(), c.member_seqs.cuda(),
+                                     c.seq_prefix.cuda(), c.block_tables.cuda(), c.context_lens.cuda(), d ** -0.5, out,
+                                     max_members=c.max_members, max_prefix_len=c.max_prefix_len,
+                                     max_context_len=max(16, int(c.context_lens.max())), scales=case[3].cuda())
+        torch.cuda.synchronize()
+    assert pkv.check_device_status() == pkv.DEVFLAG_BAD_BLOCK_ID
+    ref = _zero_block_reference(case, d, [(0, 3), (1, 7)])
+    got = out.cpu().double().numpy()
+    assert_close(got, ref, "fp8", f"{kind} pass, out-of-pool prefix blocks")
+    assert_close(got, ref, fp16_weight_atol(e4m3_vmax(case[2].numpy(), case[3].numpy())),
+                 f"{kind} pass, out-of-pool prefix blocks, fp16 weights")
+
+
+def test_e4m3_decode_out_of_pool_block_reads_zeros_and_is_flagged(pkv):
+    """The E4M3 decode (codes read straight into the MMA fragments from swizzled tiles) reads
+    a block id past the pool, or a negative one, as zeros and flags it."""
+    c, k8, v8, scales, q, full, lens = build_groups(2, 4, 128, [(6, 10)], seed=2600, own_range=(20, 70))
+    nb = k8.shape[0]
+    tb = full.clone()
+    tb[0, 2] = nb
+    tb[3, 12] = -1
+    d = 128
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    pkv.paged_decode_attention(q.cuda(), k8.cuda(), v8.cuda(), tb.cuda(), lens.cuda(), d ** -0.5, out,
+                               scales=scales.cuda(), max_context_len=int(lens.max()))
+    torch.cuda.synchronize()
+    assert pkv.check_device_status() == pkv.DEVFLAG_BAD_BLOCK_ID
+    kz = torch.cat([k8, torch.zeros_like(k8[:1])])
+    vz = torch.cat([v8, torch.zeros_like(v8[:1])])
+    tz = tb.clone()
+    tz[0, 2] = nb
+    tz[3, 12] = nb
+    ref = oracle.decode_all(W.bf16_bits(q), kz.numpy(), vz.numpy(), oracle.KV_E4M3, tz.numpy(), lens.numpy(),
+                            d ** -0.5, scales=scales.numpy())
+    assert_close(out.cpu().double().numpy(), ref, "fp32", "E4M3 decode, out-of-pool blocks")
