@@ -7,7 +7,7 @@
 // sum 2^(m_j - M) l_j (scores in log2 units).  The decode kernels write one record
 // (m, l, o) per context partition (and the prefix pass one per prefix split) and exit;
 // this kernel, launched right after them, merges the records of every (sequence, kv head)
-// that has more than one partition.  One CTA of 8 warps per (kv head, sequence, group of
+// that has more than one partition.  One CTA of up to 8 warps per (kv head, sequence, group of
 // query heads), W warps per query head (W grows with the record count, so that a warp
 // takes at most about 8 records); every load is issued before its value is needed.  The
 // records are taken in record order within a warp, the warps' partial sums are added in
@@ -158,9 +158,12 @@ static cudaError_t launch_merge_d(int g, const DecodeParams& p0, dim3 grid, cuda
   while (w < 8 && w * 8 < p.rec_slots) w *= 2;
   p.merge_warps = w;
   grid.z = static_cast<unsigned>((g + 8 / w - 1) / (8 / w));
+  // the warps a CTA uses: g * w when that is below 8 (a query group of 4 with one warp per
+  // head: 4 warps, so that twice as many CTAs fit an SM)
+  const int warps = g * w < 8 ? g * w : 8;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(256, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(32 * warps), 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
