@@ -521,7 +521,9 @@ def run_ours(args):
         if cas is not None:
             inputs.update({"c_" + k: getattr(cas, k) for k in tm.ct})
         # the step's inputs staged in one pinned host buffer (256-byte aligned fields), copied
-        # to the device in one transfer per step; the calls take device views into it
+        # to the device in one transfer per step by the SMs (pkv_stage_copy: a copy-engine
+        # transfer of this size costs about 10 us of latency); the calls take device views
+        # into it, and the output comes back the same way
         offs, total = {}, 0
         for k, v in inputs.items():
             offs[k] = total
@@ -538,7 +540,7 @@ def run_ours(args):
         d2h = h_out.numel() * h_out.element_size()
 
         def e2e_step():
-            d_pack.copy_(h_pack, non_blocking=True)
+            pkv.stage_copy(d_pack, h_pack)
             if cas is None:
                 tm.fused_step(dev_in)
             else:
@@ -546,7 +548,7 @@ def run_ours(args):
                                     tm.t["v_cache"], scales=tm.t["scales"])
                 ctabs = {k[2:]: v for k, v in dev_in.items() if k.startswith("c_")}
                 tm.decode(dev_in["q"], dev_in["tables"], dev_in["lens"], ctabs)
-            h_out.copy_(tm.out, non_blocking=True)
+            pkv.stage_copy(h_out, tm.out)
 
         for _ in range(args.warmup):
             e2e_step()
@@ -556,7 +558,7 @@ def run_ours(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e2e_ms / args.steps, 4),
                "seq_steps_per_s": round(B * ws * args.steps / (e2e_ms * 1e-3), 1)}
-        launches += user_launches * args.steps
+        launches += (user_launches + 2) * args.steps  # the step and its two staging copies
     head_partition = pkv.partition_tokens(B, hkv, max_len)
     del tm
     torch.cuda.empty_cache()
@@ -636,7 +638,7 @@ def run_ours(args):
                   "append, then the cascade call); two_call_step_us: events around append + decode as two calls; "
                   "decode_us: events around the decode alone (the two calls with an event between them); read_ceiling: events around the read-only checksum pass over the "
                   "same tables; e2e: events around one H2D copy of the step's inputs (staged in one pinned "
-                  "buffer) + append + decode + the D2H of the output; each timed step follows an untimed L2 flush "
+                  "buffer, copied by the SMs: pkv_stage_copy) + the step + the D2H of the output (the same way); each timed step follows an untimed L2 flush "
                   "and an untimed GPU spin that lets the host queue the step first; configs: the other target "
                   "workloads under the same protocol",
         "clocks": clocks,

@@ -318,6 +318,23 @@ pkv_status pkv_paged_kv_checksum(const pkv_cache_desc* cache, const int32_t* blo
                                  int32_t max_context_len, uint32_t* checksums, pkv_stream_t stream);
 
 /*
+ * Copy `bytes` bytes from src to dst with the SMs, in order with the work on `stream`.
+ * (The pages describe no such call.  It moves a decode step's inputs from page-locked host
+ * memory to the device and its output back: on GB300 a copy-engine transfer of a few
+ * hundred KiB costs about 10 us, nearly all latency, where the SMs read or write page-locked
+ * host memory directly over the host link in a few.)
+ *   dst, src: device memory or page-locked host memory (cudaHostAlloc, cudaHostRegister,
+ *     or a pinned tensor: the same pointer addresses it on the device); both 16-byte
+ *     aligned; the two ranges must not overlap.
+ *   bytes: a multiple of 16; 0 is a no-op.
+ * The copy starts once the work queued on `stream` before it has completed, and lets the
+ * next kernel's launch proceed meanwhile (programmatic dependent launch).  Errors: a NULL or
+ * misaligned pointer, a size not a multiple of 16 or overlapping ranges give
+ * PKV_ERR_INVALID_ARG before any CUDA call.
+ */
+pkv_status pkv_stage_copy(void* dst, const void* src, size_t bytes, pkv_stream_t stream);
+
+/*
  * Read and clear the device status word of the current device after the work queued on
  * `stream` so far has finished (this call synchronises `stream`).  *flags receives the
  * PKV_DEVFLAG_* bits (may be NULL).  Returns PKV_ERR_DEVICE_CHECK if any bit was set,

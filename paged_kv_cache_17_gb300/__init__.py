@@ -45,7 +45,7 @@ EXPORTED_SYMBOLS = (
     "pkv_decode_partition_tokens", "pkv_paged_decode_attention", "pkv_check_device_status",
     "pkv_status_string", "pkv_last_error", "pkv_version", "pkv_paged_decode_attention_noalloc",
     "pkv_copy_blocks", "pkv_cascade_workspace_size", "pkv_cascade_decode_attention", "pkv_paged_kv_checksum",
-    "pkv_paged_append_decode",
+    "pkv_paged_append_decode", "pkv_stage_copy",
 )
 
 
@@ -98,6 +98,8 @@ def _load() -> ctypes.CDLL:
     lib.pkv_paged_kv_checksum.argtypes = [ctypes.POINTER(CacheDesc), P, i32, P, i32, i32, P, P]
     lib.pkv_copy_blocks.restype = ctypes.c_int
     lib.pkv_copy_blocks.argtypes = [ctypes.POINTER(CacheDesc), P, i64, P]
+    lib.pkv_stage_copy.restype = ctypes.c_int
+    lib.pkv_stage_copy.argtypes = [P, P, ctypes.c_size_t, P]
     lib.pkv_check_device_status.restype = ctypes.c_int
     lib.pkv_check_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -371,6 +373,22 @@ def kv_checksum(k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torc
     _check(lib.pkv_paged_kv_checksum(ctypes.byref(desc), block_tables.data_ptr(), block_tables.shape[1],
                                      context_lens.data_ptr(), B, max_context_len, out.data_ptr(), _stream(stream)))
     return out
+
+
+def stage_copy(dst: torch.Tensor, src: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Copy src into dst with the SMs (include/pkv.h pkv_stage_copy): either may be a
+    page-locked (pinned) CPU tensor or a tensor on the current device; both contiguous, of
+    the same number of bytes (a multiple of 16), 16-byte aligned."""
+    for name, t in (("dst", dst), ("src", src)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device.type == "cpu" and not t.is_pinned():
+            raise ValueError(f"{name} must be a pinned (page-locked) CPU tensor or a CUDA tensor")
+    n = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != n:
+        raise ValueError("dst and src must hold the same number of bytes")
+    _check(lib.pkv_stage_copy(dst.data_ptr(), src.data_ptr(), n, _stream(stream)))
+    return dst
 
 
 def check_device_status(stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -19,7 +19,7 @@ LIB = os.path.join(OUT_DIR, "libpkv.so")
 SOURCES = ["pkv_api.cu", "append.cu", "decode_bf16.cu", "decode_e4m3.cu", "pkv_noalloc.cu", "copy_blocks.cu",
            "block_manager.cpp", "cascade_bf16.cu", "cascade_e4m3.cu",
            "decode_mma.cu", "decode_mma_e4m3.cu",
-           "merge_partitions.cu", "cascade_prefix_tc.cu", "cascade_prefix_mma.cu", "kv_checksum.cu"]
+           "merge_partitions.cu", "cascade_prefix_tc.cu", "cascade_prefix_mma.cu", "kv_checksum.cu", "stage_copy.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

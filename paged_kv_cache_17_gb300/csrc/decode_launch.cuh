@@ -165,6 +165,9 @@ struct ChecksumParams {
   int max_context_len;
   int split_blocks;
 };
+// copy `bytes` (a multiple of 16) with the SMs; either side may be page-locked host memory
+cudaError_t launch_stage_copy(void* dst, const void* src, size_t bytes, int sm_count, cudaStream_t stream);
+
 cudaError_t launch_kv_checksum(int row_bytes, const CUtensorMap& tk, const CUtensorMap& tv, const ChecksumParams& p,
                                dim3 grid, cudaStream_t stream);
 

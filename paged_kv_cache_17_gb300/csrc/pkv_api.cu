@@ -794,6 +794,22 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
                        pp.pre_slots);
 }
 
+pkv_status pkv_stage_copy(void* dst, const void* src, size_t bytes, pkv_stream_t stream) {
+  t_last_error.clear();
+  if (bytes == 0) return PKV_OK;
+  if (!dst || !src) return fail(PKV_ERR_INVALID_ARG, "dst and src must be non-NULL");
+  if (!aligned(dst, 16) || !aligned(src, 16)) return fail(PKV_ERR_INVALID_ARG, "dst and src must be 16-byte aligned");
+  if (bytes % 16 != 0) return fail(PKV_ERR_INVALID_ARG, "bytes (%zu) must be a multiple of 16", bytes);
+  const uintptr_t d = reinterpret_cast<uintptr_t>(dst), s = reinterpret_cast<uintptr_t>(src);
+  if (d < s + bytes && s < d + bytes) return fail(PKV_ERR_INVALID_ARG, "dst and src overlap");
+  DeviceInfo* dev = nullptr;
+  pkv_status st = device_info(&dev);
+  if (st != PKV_OK) return st;
+  const cudaError_t e = pkv::launch_stage_copy(dst, src, bytes, dev->sm_count, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stage copy launch");
+  return PKV_OK;
+}
+
 pkv_status pkv_paged_kv_checksum(const pkv_cache_desc* cache, const int32_t* block_tables,
                                  int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t batch,
                                  int32_t max_context_len, uint32_t* checksums, pkv_stream_t stream) {

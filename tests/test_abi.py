@@ -134,3 +134,16 @@ def test_noalloc_refusals_match_the_regular_entry_point_on_host(pkv):
         st_na = pkv.lib.pkv_paged_decode_attention_noalloc(*args, None)
         assert st_reg == want, (dkw, ckw, st_reg, msg_reg)
         assert st_na == st_reg and last(pkv) == msg_reg, (dkw, ckw, st_na, last(pkv), msg_reg)
+
+
+def test_stage_copy_refuses_bad_arguments_on_host(pkv):
+    """The staging copy checks its pointers and size before any CUDA call."""
+    sc = pkv.lib.pkv_stage_copy
+    assert sc(0x10000, 0x20000, 0, None) == pkv.PKV_OK  # nothing to copy
+    assert sc(None, 0x20000, 16, None) == pkv.PKV_ERR_INVALID_ARG
+    assert sc(0x10000, None, 16, None) == pkv.PKV_ERR_INVALID_ARG
+    assert sc(0x10008, 0x20000, 16, None) == pkv.PKV_ERR_INVALID_ARG and "aligned" in last(pkv)
+    assert sc(0x10000, 0x20004, 16, None) == pkv.PKV_ERR_INVALID_ARG
+    assert sc(0x10000, 0x20000, 24, None) == pkv.PKV_ERR_INVALID_ARG and "multiple of 16" in last(pkv)
+    assert sc(0x10000, 0x10010, 64, None) == pkv.PKV_ERR_INVALID_ARG and "overlap" in last(pkv)
+    assert sc(0x10010, 0x10000, 64, None) == pkv.PKV_ERR_INVALID_ARG

@@ -49,8 +49,9 @@ def test_bench_line_plain_decode():
     plus the read-only ceiling pass (one launch per timed step)."""
     d = run_bench("--config", "tiny", "--steps", "5", "--warmup", "3", "--cpu-seconds", "1", "--no-extra-configs")
     check_contract(d, 5, 3)
-    # fused step (1) + decode pass (append + decode: 2) + two-call pass (2) + e2e (1), per step; the read pass
-    assert d["gpu_launches"] == (1 + 2 + 2 + 1) * 5 + 5
+    # fused step (1) + decode pass (append + decode: 2) + two-call pass (2) + e2e (the fused step
+    # and its two staging copies: 3), per step; the read pass
+    assert d["gpu_launches"] == (1 + 2 + 2 + 3) * 5 + 5
     assert d["two_call_step_us"] > 0 and "paged_append_decode" in d["step_call"]
     rc = d["read_ceiling"]
     assert rc["us"] > 0 and rc["gbs"] > 0 and abs(rc["frac"] - rc["gbs"] / d["roofline"]["peak"]) < 1e-3
@@ -63,7 +64,8 @@ def test_bench_line_cascade():
     d = run_bench("--config", "prefix_shared", "--cascade", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1",
                   "--no-extra-configs")
     check_contract(d, 3, 3)
-    assert d["gpu_launches"] == 4 * 3 * 3  # append, prefix pass, decode, merge: three timed passes
+    # append, prefix pass, decode, merge: three timed passes, the e2e one with two staging copies
+    assert d["gpu_launches"] == 4 * 3 * 3 + 2 * 3
     assert "cascade_prefix_tc_kernel" in d["roofline"]["kernel"]
 
 
