@@ -21,7 +21,7 @@
 //     both q and K leaves unchanged; lane (gid, tig) takes dims tig*D/4 .. +D/4 of every
 //     k-step's pairs, so its K operand is D/4 consecutive codes of token gid (one or two
 //     16-byte loads), and cvt.rn.f16x2.e4m3x2 turns each code pair into one fragment
-//     register; q takes the same permutation once, in registers;
+//     register; q takes the same permutation once (ready-made A fragments in shared memory);
 //   - the output product's column n of n-tile j is dim n*D/8 + j, so a lane's V operand is
 //     D/8 consecutive codes of each of its four tokens; byte permutes pair the codes of two
 //     tokens before the expansion; the output rows come back with the same map.
@@ -40,7 +40,9 @@
 // slot one iteration after reading it, when the other slice has released it too.  A stage
 // is read into registers and released before the arithmetic.  q sits in shared memory as
 // ready-made A fragments.  At the end the warps of a slice combine their (m, l, O) through
-// shared memory and one of them writes the split's record per row.
+// shared memory and one of them writes the split's record per row.  128 registers and 42 KiB
+// (D = 128, 32 rows): four CTAs fit an SM; the host plans two, so that decode CTAs stream the
+// sequences' own blocks beside the pass.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
