@@ -111,6 +111,17 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
 
+  // the barriers need no global memory: set them up before waiting for the previous grid
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], MT);  // the warps of every slice read each stage
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
   pdl_wait();
   // the decode kernel that follows may start now: what it reads before waiting for this
   // grid (the pool after the append) is complete once every CTA is past the wait above
@@ -135,8 +146,43 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
   const int nloc = min(pblocks, blk0 + p.split_blocks) - blk0;
   const int32_t* table = p.prefix_tables + static_cast<size_t>(pfx) * p.max_prefix_blocks + blk0;
 
-  // ---- this warp's rows: slice mt, rows 16 mt + gid and 16 mt + gid + 8
   const int mt = warp % MT, st = warp / MT;
+  // ---- this warp's stream: stream-local stage k is block st + k NS of the split, in slot
+  // st + (k mod DEPTH) NS of the ring; the slice-0 warp's lane 0 loads it
+  const int nk = nloc > st ? (nloc - st + NS - 1) / NS : 0;
+  const bool loader = mt == 0;
+  auto slot = [&](int k) { return st + (k % DEPTH) * NS; };
+  int ids_cur = 0, ids_next = 0;  // loader: block ids of stream stages 32 j + lane, 32 (j + 1) + lane
+  if (loader) {
+    ids_cur = lane < nk ? table[st + lane * NS] : 0;
+    ids_next = 32 + lane < nk ? table[st + (32 + lane) * NS] : 0;
+  }
+  int issued = 0;  // loader: stream stages issued so far
+  auto issue = [&]() {  // the loader warp, converged: load stream stage `issued`
+    const int k = issued;
+    if (k > 0 && k % 32 == 0) {
+      ids_cur = ids_next;
+      ids_next = k + 32 + lane < nk ? table[st + (k + 32 + lane) * NS] : 0;
+    }
+    const int pb = __shfl_sync(kFull, ids_cur, k % 32);
+    if (lane == 0) {
+      const int sg = slot(k);
+      const bool ok = pb >= 0 && pb < p.num_blocks;
+      if (!ok) set_flag(p.status, PKV_DEVFLAG_BAD_BLOCK_ID);
+      // an id outside the pool reads a box entirely outside the tensor: zeros
+      const int row0 = ok ? pb * kBlockSize : -kBlockSize;
+      mbar_arrive_expect_tx(&full_bar[sg], 2 * C::kTile);
+      tma_load_3d(k_tiles + sg * C::kTile, &tm_k, 0, h, row0, &full_bar[sg]);
+      tma_load_3d(v_tiles + sg * C::kTile, &tm_v, 0, h, row0, &full_bar[sg]);
+    }
+    issued = k + 1;
+  };
+  // the first loads go out now, before the member rows and q are read (their round trips
+  // overlap the loads' latency)
+  if (loader)
+    while (issued < min(DEPTH, nk)) issue();
+
+  // ---- this warp's rows: slice mt, rows 16 mt + gid and 16 mt + gid + 8
   int rb[2] = {0, 0}, rg[2] = {0, 0};
   bool rv[2] = {false, false};
 #pragma unroll
@@ -215,49 +261,7 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
       for (int kk = 0; kk < KS; ++kk) qs[(mt * KS + kk) * 32 + lane] = make_uint4(qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
     }
   }
-  if (threadIdx.x == 0) {
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], MT);  // the warps of every slice read each stage
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  // ---- this warp's stream: stream-local stage k is block st + k NS of the split, in slot
-  // st + (k mod DEPTH) NS of the ring; the slice-0 warp's lane 0 loads it
-  const int nk = nloc > st ? (nloc - st + NS - 1) / NS : 0;
-  const bool loader = mt == 0;
-  auto slot = [&](int k) { return st + (k % DEPTH) * NS; };
-  int ids_cur = 0, ids_next = 0;  // loader: block ids of stream stages 32 j + lane, 32 (j + 1) + lane
-  if (loader) {
-    ids_cur = lane < nk ? table[st + lane * NS] : 0;
-    ids_next = 32 + lane < nk ? table[st + (32 + lane) * NS] : 0;
-  }
-  int issued = 0;  // loader: stream stages issued so far
-  auto issue = [&]() {  // the loader warp, converged: load stream stage `issued`
-    const int k = issued;
-    if (k > 0 && k % 32 == 0) {
-      ids_cur = ids_next;
-      ids_next = k + 32 + lane < nk ? table[st + (k + 32 + lane) * NS] : 0;
-    }
-    const int pb = __shfl_sync(kFull, ids_cur, k % 32);
-    if (lane == 0) {
-      const int sg = slot(k);
-      const bool ok = pb >= 0 && pb < p.num_blocks;
-      if (!ok) set_flag(p.status, PKV_DEVFLAG_BAD_BLOCK_ID);
-      // an id outside the pool reads a box entirely outside the tensor: zeros
-      const int row0 = ok ? pb * kBlockSize : -kBlockSize;
-      mbar_arrive_expect_tx(&full_bar[sg], 2 * C::kTile);
-      tma_load_3d(k_tiles + sg * C::kTile, &tm_k, 0, h, row0, &full_bar[sg]);
-      tma_load_3d(v_tiles + sg * C::kTile, &tm_v, 0, h, row0, &full_bar[sg]);
-    }
-    issued = k + 1;
-  };
-  if (loader)
-    while (issued < min(DEPTH, nk)) issue();
+  __syncthreads();  // the q fragments are in shared memory
 
   // per lane: rows gid (e = 0, 1) and gid + 8 (e = 2, 3) of the slice; o[j] holds dims
   // (2 tig) D/8 + j (e = 0, 2) and (2 tig + 1) D/8 + j (e = 1, 3)
