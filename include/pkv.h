@@ -330,7 +330,8 @@ pkv_status pkv_paged_kv_checksum(const pkv_cache_desc* cache, const int32_t* blo
  * The copy starts once the work queued on `stream` before it has completed, and lets the
  * next kernel's launch proceed meanwhile (programmatic dependent launch).  Errors: a NULL or
  * misaligned pointer, a size not a multiple of 16 or overlapping ranges give
- * PKV_ERR_INVALID_ARG before any CUDA call.
+ * PKV_ERR_INVALID_ARG before any CUDA call; so does a pointer to memory that is neither
+ * device, page-locked host nor managed memory (checked with the runtime's pointer query).
  */
 pkv_status pkv_stage_copy(void* dst, const void* src, size_t bytes, pkv_stream_t stream);
 

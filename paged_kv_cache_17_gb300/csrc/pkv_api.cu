@@ -805,6 +805,17 @@ pkv_status pkv_stage_copy(void* dst, const void* src, size_t bytes, pkv_stream_t
   DeviceInfo* dev = nullptr;
   pkv_status st = device_info(&dev);
   if (st != PKV_OK) return st;
+  // both sides must be memory the device addresses: device, page-locked host or managed
+  // memory (ordinary host memory is refused here rather than faulting in the kernel)
+  for (const void* ptr : {static_cast<const void*>(dst), src}) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(PKV_ERR_INVALID_ARG, "cannot query the memory behind %p", ptr);
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeHost && a.type != cudaMemoryTypeManaged)
+      return fail(PKV_ERR_INVALID_ARG, "%p is neither device nor page-locked host memory", ptr);
+  }
   const cudaError_t e = pkv::launch_stage_copy(dst, src, bytes, dev->sm_count, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stage copy launch");
   return PKV_OK;

@@ -58,3 +58,22 @@ def test_refusals(pkv):
         pkv.stage_copy(d, torch.zeros(48, dtype=torch.uint8, device="cuda"))
     with pytest.raises(pkv.PkvError):
         pkv.stage_copy(d[:24], torch.zeros(24, dtype=torch.uint8, device="cuda"))
+
+
+def test_ordinary_host_memory_is_refused(pkv):
+    """Host memory that is not page-locked is refused on the host (no kernel runs)."""
+    import ctypes
+
+    import numpy as np
+
+    host = np.zeros(4096, dtype=np.uint8)  # ordinary, unregistered host memory
+    base = host.ctypes.data
+    ptr = (base + 15) // 16 * 16
+    d = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    st = pkv.lib.pkv_stage_copy(d.data_ptr(), ctypes.c_void_p(ptr), 1024, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG and "page-locked" in pkv.lib.pkv_last_error().decode()
+    st = pkv.lib.pkv_stage_copy(ctypes.c_void_p(ptr), d.data_ptr(), 1024, None)
+    assert st == pkv.PKV_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert pkv.check_device_status() == 0
+
