@@ -125,6 +125,28 @@ def test_decode_multi_partition(split):
     _check_flags()
 
 
+@pytest.mark.parametrize("split", [None, 16, 64])
+@pytest.mark.parametrize("d,g", [(64, 1), (64, 2), (64, 4), (64, 8), (128, 1), (128, 2), (128, 4), (128, 8)])
+def test_e4m3_decode_every_group_size_and_partitions(d, g, split):
+    """The E4M3 decode reads its codes from 128-byte (D = 128) or 64-byte (D = 64) swizzled
+    tiles straight into the MMA fragments (head-dim permutation for K, byte-permuted token
+    pairs for V): every query-group instance, one partition per sequence and 16- or 64-token
+    partitions (the merge kernel), lengths 1..300 with partial last blocks."""
+    hkv = 2
+    cfg = W.Config(name="e4m3_groups", hq=hkv * g, hkv=hkv, d=d, kv_dtype="e4m3", softmax_scale=1.0 / np.sqrt(d),
+                   seed=400 + d + 10 * g, kind="uniform", batch=10, len_range=(1, 300))
+    w = W.make_workload(cfg)
+    with split_tokens(split):
+        _, out = gpu_step(w)
+    a, kc, vc = oracle_pools_after_append(w)
+    ref = oracle.decode_all(a["q"], kc, vc, oracle.KV_E4M3, a["block_tables"], a["context_lens"], cfg.softmax_scale,
+                            scales=a["scales"], nthreads=NT)
+    got = out.cpu().double().numpy()
+    assert_close(got, ref, "fp8", f"e4m3 d={d} g={g} split={split}")
+    assert_close(got, ref, "fp32", f"e4m3 d={d} g={g} split={split}")
+    _check_flags()
+
+
 @pytest.mark.parametrize("d,g,kv", [(64, 1, "bf16"), (64, 2, "bf16"), (64, 4, "e4m3"), (64, 8, "bf16"),
                                     (128, 1, "e4m3"), (128, 2, "bf16"), (128, 4, "bf16"), (128, 8, "e4m3")])
 def test_decode_edge_lengths_all_variants(d, g, kv):
