@@ -248,8 +248,10 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const
  * (prefix blocks of sequence b, if any) then (the blocks of block_tables row b), exactly
  * as pkv_paged_decode_attention over that concatenated table computes it, up to fp32
  * rounding.  The prefix part is computed once per prefix for all its member sequences,
- * as a dense [members x G rows] x [prefix keys] contraction on the fifth-generation tensor
- * cores (tcgen05 MMAs of 128 query rows, fp32 accumulation in tensor memory); the
+ * as a dense [members x G rows] x [prefix keys] contraction: on the fifth-generation tensor
+ * cores (tcgen05 MMAs of 128 query rows, fp32 accumulation in tensor memory), or, for an
+ * E4M3 pool whose groups hold at most 32 query rows (max_members x G <= 32), on mma.sync
+ * tensor-core tiles of 16 rows that expand the codes straight into their operands; the
  * sequences' own blocks go through the decode kernel, and the prefix results are merged
  * with log-sum-exp weights by a merge kernel after the decode (so that no decode CTA waits
  * for the prefix pass; for bf16 pools the pass runs beside the decode).
@@ -262,12 +264,15 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const
  *   Arithmetic of the prefix part: bf16 pools multiply bf16 q and K, and the softmax
  *   weights enter the P V product as a bf16 hi + lo pair (about 16 significant bits);
  *   E4M3 pools expand the codes exactly to fp16, multiply fp16 q (q rounded to fp16, exact
- *   for |q| in 2^-14 .. 65504) and fp16 weights, whose rounded sum is the denominator.
+ *   for |q| in 2^-14 .. 65504) and fp16 weights; the tcgen05 pass sums the rounded weights
+ *   into the denominator, the mma.sync pass the fp32 weights before rounding (either way
+ *   each weight's relative error is at most 2^-11).
  *   Tuning (environment, read at each call; results agree within the tolerances above):
  *   PKV_PREFIX_SPLIT_BLOCKS (>= 4) fixes the prefix blocks per split of the prefix pass,
  *   PKV_PREFIX_CTAS_PER_SM (1 or 2) the prefix-pass CTAs an SM is planned for, and
  *   PKV_CASCADE_DEFER (0 or 1) whether the prefix records are merged in the decode kernel (0)
- *   or by the merge kernel after it (1); PKV_SPLIT_TOKENS applies as for the plain decode.
+ *   or by the merge kernel after it (1), and PKV_PREFIX_PASS ("tc" or "mma") which prefix
+ *   pass runs where both apply; PKV_SPLIT_TOKENS applies as for the plain decode.
  */
 typedef struct {
   const int32_t* prefix_tables;  /* [num_prefixes][max_prefix_blocks] physical block ids */
