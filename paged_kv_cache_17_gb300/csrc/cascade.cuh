@@ -29,6 +29,8 @@ struct PrefixParams {
   int rec_slots;    // records per (sequence, kv head): pre_slots + decode partitions
   float score_scale;  // softmax_scale * log2(e)
   const float* scales;  // [2][Hkv] (E4M3 pools) or nullptr
+  const uint8_t* k_codes;  // the pools (read by the mma.sync pass without tensor maps)
+  const uint8_t* v_codes;
 };
 
 
@@ -52,17 +54,14 @@ PKV_DECLARE_PREFIX_TC(128, true)
 
 // The prefix pass for small member groups of an E4M3 pool on mma.sync
 // (cascade_prefix_mma.cu): at most 16 MT query rows per (prefix, kv head), grid.x = 1; the
-// pools are read through tensor maps of 16 rows x D codes with the 128-byte (D = 128) or
-// 64-byte (D = 64) swizzle.
+// warps copy the pool's codes (k_codes / v_codes) into their rings themselves.
 template <int D, int MT>
 int cascade_prefix_mma_ctas_per_sm(int device);  // CTAs of the pass resident per SM; 0 on error
 template <int D, int MT>
-cudaError_t launch_cascade_prefix_mma(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p, dim3 grid,
-                                      cudaStream_t stream, int device);
-#define PKV_DECLARE_PREFIX_MMA(D, MT)                                                                        \
-  extern template int cascade_prefix_mma_ctas_per_sm<D, MT>(int);                                           \
-  extern template cudaError_t launch_cascade_prefix_mma<D, MT>(const CUtensorMap&, const CUtensorMap&,      \
-                                                               const PrefixParams&, dim3, cudaStream_t, int);
+cudaError_t launch_cascade_prefix_mma(const PrefixParams& p, dim3 grid, cudaStream_t stream, int device);
+#define PKV_DECLARE_PREFIX_MMA(D, MT)                                              \
+  extern template int cascade_prefix_mma_ctas_per_sm<D, MT>(int);                 \
+  extern template cudaError_t launch_cascade_prefix_mma<D, MT>(const PrefixParams&, dim3, cudaStream_t, int);
 PKV_DECLARE_PREFIX_MMA(64, 1)
 PKV_DECLARE_PREFIX_MMA(64, 2)
 PKV_DECLARE_PREFIX_MMA(128, 1)

@@ -16,7 +16,7 @@
 //                                                  operand of the next product as they are)
 //   O [16 x D]            += P [16 x 16] V [16 x D]
 //
-// The codes go from the TMA tile straight into the MMA fragments, with no expanded copy:
+// The codes go from the staged tile straight into the MMA fragments, with no expanded copy:
 //   - the score product contracts over the head dimension, which any permutation applied to
 //     both q and K leaves unchanged; lane (gid, tig) takes dims tig*D/4 .. +D/4 of every
 //     k-step's pairs, so its K operand is D/4 consecutive codes of token gid (one or two
@@ -25,8 +25,9 @@
 //   - the output product's column n of n-tile j is dim n*D/8 + j, so a lane's V operand is
 //     D/8 consecutive codes of each of its four tokens; byte permutes pair the codes of two
 //     tokens before the expansion; the output rows come back with the same map.
-// The tiles are loaded with the 128-byte (D = 128) or 64-byte (D = 64) TMA swizzle, under
-// which these loads meet no bank conflicts.  E4M3 codes expand to fp16 exactly; q is scaled
+// The tiles are stored with the 128-byte (D = 128) or 64-byte (D = 64) swizzle (16-byte
+// chunk c of row r at chunk c ^ (r mod 8), or c ^ ((r / 2) mod 4)), under which these loads
+// meet no bank conflicts.  E4M3 codes expand to fp16 exactly; q is scaled
 // per row by a power of two into fp16's range (folded into the row's score scale with the
 // K scale), the weights are fp16, and the V scale is applied by the merge kernel.  The
 // reference max of a row moves only when a block's max exceeds it by more than 2^8, so the
@@ -35,14 +36,17 @@
 // CTA = one (kv head, prefix, split of the prefix's blocks), four warps and no producer
 // warp (its registers would cost a CTA per SM): warp w takes the 16-row slice w % MT of the
 // group and the block stream w / MT, i.e. blocks w / MT, w / MT + 4 / MT, ...; each stream
-// has four slots of a ring of 16-token K and V tiles, and lane 0 of the stream's slice-0
-// warp keeps them filled by TMA (block ids 32 at a time in its warp's lanes), refilling a
-// slot one iteration after reading it, when the other slice has released it too.  A stage
-// is read into registers and released before the arithmetic.  q sits in shared memory as
-// ready-made A fragments.  At the end the warps of a slice combine their (m, l, O) through
-// shared memory and one of them writes the split's record per row.  128 registers and 42 KiB
-// (D = 128, 32 rows): four CTAs fit an SM; the host plans two, so that decode CTAs stream the
-// sequences' own blocks beside the pass.
+// has four slots of a ring of 16-token K and V tiles, which the stream's own MT warps fill
+// with 16-byte cp.async copies (block ids 32 at a time in every warp's lanes).  Per block:
+// wait for this thread's copies of the block, meet the other slice's warp at the stream's
+// named barrier (its copies have landed, and it has read the previous block), refill the
+// previous block's slot with the block DEPTH - 1 ahead, then compute from the tile.  No
+// thread waits on another thread's flag, and no single lane issues the copies (a loading
+// lane's tensor-map copies had stood on every block's critical path).  q sits in shared
+// memory as ready-made A fragments.  At the end the warps of a slice combine their (m, l, O)
+// through shared memory and one of them writes the split's record per row.  128 registers
+// and 40 KiB (D = 128, 32 rows): four CTAs fit an SM; the host plans two, so that decode
+// CTAs stream the sequences' own blocks beside the pass.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -62,6 +66,10 @@ struct MmaPrefixCfg {
   static constexpr int kDepth = 4;                     // ring slots per stream
   static constexpr int kStages = kDepth * kStreams;
   static constexpr int kTile = kBlockSize * D;         // one K or V tile of codes
+  static constexpr int kRowChunks = D / 16;            // 16-byte chunks of a token's codes
+  static constexpr int kTileChunks = kBlockSize * kRowChunks;
+  static constexpr int kCopyThreads = 32 * MT;         // the warps of a stream copy its stages
+  static constexpr int kTileCopies = kTileChunks / kCopyThreads;  // per thread and tile
   static constexpr int kKS = D / 16;                   // k-steps of the score product
   static constexpr int kNT = D / 8;                    // n-tiles of the output product
   static constexpr int kDQ = D / 4;                    // score-product dims per lane
@@ -69,14 +77,13 @@ struct MmaPrefixCfg {
   static constexpr int kScratchBytes = (kStreams - 1) * MT * 32 * kFrag * 4;
   static constexpr int kRingBytes = 2 * kStages * kTile;
   static constexpr int kOffQ = kRingBytes;             // q fragments [slice][k-step][lane] x 16 B
-  static constexpr int kOffBar = kOffQ + MT * kKS * 32 * 16;
-  static constexpr int kSmemBytes = 1024 + kOffBar + 2 * kStages * 8;  // 1024: alignment slack
+  static constexpr int kSmemBytes = kOffQ + MT * kKS * 32 * 16;
   static constexpr int kMinCtas = 4;                   // CTAs per SM the registers are capped for
   static constexpr float kLazy = 8.f;                  // log2 of the largest weight before a rescale
   static_assert(D == 64 || D == 128, "head_dim");
   static_assert(MT == 1 || MT == 2, "16 or 32 query rows");
   static_assert(kScratchBytes <= kRingBytes, "the merge scratch reuses the ring");
-  static_assert(kRingBytes % 1024 == 0 && kTile % 512 == 0, "swizzle-aligned tiles");
+  static_assert(kTileChunks % kCopyThreads == 0 && kTileCopies >= 1, "whole copies per thread");
 };
 
 namespace {
@@ -88,22 +95,42 @@ __device__ __forceinline__ float exp2_ftz(float x) {
   return y;
 }
 
+// 16 bytes global -> shared through L2 only; with valid false nothing is read and the
+// destination is zero-filled
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// the warps of one block stream meet: barrier 1 + stream among its MT warps (two streams
+// when MT = 2)
+template <int MT>
+__device__ __forceinline__ void stream_sync(int st) {
+  if constexpr (MT == 1) {
+    __syncwarp();
+  } else {
+    static_assert(MT == 2, "two streams of two warps");
+    if (st == 0) asm volatile("bar.sync 1, 64;" ::: "memory");
+    else asm volatile("bar.sync 2, 64;" ::: "memory");
+  }
+}
+
 }  // namespace
 
 template <int D, int MT>
 __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D, MT>::kMinCtas)
-    cascade_prefix_mma_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                              const PrefixParams p) {
+    cascade_prefix_mma_kernel(const PrefixParams p) {
   using C = MmaPrefixCfg<D, MT>;
   constexpr int KS = C::kKS, NT = C::kNT, NS = C::kStreams, DEPTH = C::kDepth;
   constexpr int KCH = C::kDQ / 16;  // 16-byte chunks of a lane's K operand per token
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* k_tiles = smem;
   uint8_t* v_tiles = smem + C::kStages * C::kTile;
   uint4* qs = reinterpret_cast<uint4*>(smem + C::kOffQ);
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* empty_bar = full_bar + C::kStages;
 
   const int h = blockIdx.y;
   const int pfx = blockIdx.z / p.pre_slots;
@@ -111,17 +138,6 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
 
-  // the barriers need no global memory: set them up before waiting for the previous grid
-  if (threadIdx.x == 0) {
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], MT);  // the warps of every slice read each stage
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
   pdl_wait();
   // the decode kernel that follows may start now: what it reads before waiting for this
   // grid (the pool after the append) is complete once every CTA is past the wait above
@@ -148,39 +164,45 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
 
   const int mt = warp % MT, st = warp / MT;
   // ---- this warp's stream: stream-local stage k is block st + k NS of the split, in slot
-  // st + (k mod DEPTH) NS of the ring; the slice-0 warp's lane 0 loads it
+  // st + (k mod DEPTH) NS of the ring, copied by the stream's MT warps together
   const int nk = nloc > st ? (nloc - st + NS - 1) / NS : 0;
-  const bool loader = mt == 0;
   auto slot = [&](int k) { return st + (k % DEPTH) * NS; };
-  int ids_cur = 0, ids_next = 0;  // loader: block ids of stream stages 32 j + lane, 32 (j + 1) + lane
-  if (loader) {
-    ids_cur = lane < nk ? table[st + lane * NS] : 0;
-    ids_next = 32 + lane < nk ? table[st + (32 + lane) * NS] : 0;
-  }
-  int issued = 0;  // loader: stream stages issued so far
-  auto issue = [&]() {  // the loader warp, converged: load stream stage `issued`
-    const int k = issued;
-    if (k > 0 && k % 32 == 0) {
-      ids_cur = ids_next;
-      ids_next = k + 32 + lane < nk ? table[st + (k + 32 + lane) * NS] : 0;
-    }
-    const int pb = __shfl_sync(kFull, ids_cur, k % 32);
-    if (lane == 0) {
-      const int sg = slot(k);
+  int ids_cur = lane < nk ? table[st + lane * NS] : 0;  // block ids of stages 32 j + lane, 32 (j + 1) + lane
+  int ids_next = 32 + lane < nk ? table[st + (32 + lane) * NS] : 0;
+  // this thread's chunks of a tile: chunk c = copy thread + i * copy threads, token c / (D/16)
+  const int ct = mt * 32 + lane;
+  const size_t tok_stride = static_cast<size_t>(p.hkv) * D;
+  // stage k of the stream (one commit group, empty past the last stage); the warps of the
+  // stream call it with the same k, converged
+  auto issue = [&](int k) {
+    if (k < nk) {
+      if (k > 0 && k % 32 == 0) {
+        ids_cur = ids_next;
+        ids_next = k + 32 + lane < nk ? table[st + (k + 32 + lane) * NS] : 0;
+      }
+      const int pb = __shfl_sync(kFull, ids_cur, k % 32);
       const bool ok = pb >= 0 && pb < p.num_blocks;
-      if (!ok) set_flag(p.status, PKV_DEVFLAG_BAD_BLOCK_ID);
-      // an id outside the pool reads a box entirely outside the tensor: zeros
-      const int row0 = ok ? pb * kBlockSize : -kBlockSize;
-      mbar_arrive_expect_tx(&full_bar[sg], 2 * C::kTile);
-      tma_load_3d(k_tiles + sg * C::kTile, &tm_k, 0, h, row0, &full_bar[sg]);
-      tma_load_3d(v_tiles + sg * C::kTile, &tm_v, 0, h, row0, &full_bar[sg]);
+      if (!ok && ct == 0) set_flag(p.status, PKV_DEVFLAG_BAD_BLOCK_ID);
+      // an id outside the pool reads nothing: the tiles are zero-filled
+      const size_t row0 = (static_cast<size_t>(ok ? pb : 0) * kBlockSize * p.hkv + h) * D;
+      uint8_t* kt = k_tiles + slot(k) * C::kTile;
+      uint8_t* vt = v_tiles + slot(k) * C::kTile;
+#pragma unroll
+      for (int i = 0; i < C::kTileCopies; ++i) {
+        const int c = ct + i * C::kCopyThreads;
+        const int tok = c / C::kRowChunks, ch = c % C::kRowChunks;
+        const size_t g = row0 + tok * tok_stride + ch * 16;
+        const int so = e4m3_off<D>(tok, ch);
+        cp_async16(kt + so, p.k_codes + g, ok);
+        cp_async16(vt + so, p.v_codes + g, ok);
+      }
     }
-    issued = k + 1;
+    cp_async_commit();
   };
-  // the first loads go out now, before the member rows and q are read (their round trips
-  // overlap the loads' latency)
-  if (loader)
-    while (issued < min(DEPTH, nk)) issue();
+  // the first DEPTH - 1 stages go out now, before the member rows and q are read (their
+  // round trips overlap the copies' latency)
+#pragma unroll
+  for (int k = 0; k < DEPTH - 1; ++k) issue(k);
 
   // ---- this warp's rows: slice mt, rows 16 mt + gid and 16 mt + gid + 8
   int rb[2] = {0, 0}, rg[2] = {0, 0};
@@ -202,7 +224,7 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
   constexpr float kVUnit = 7.52316384526264e-37f;  // 2^-120: the decode kernel's E4M3 record units
   auto record = [&](int i) { return ((static_cast<size_t>(rb[i]) * p.hkv + h) * p.rec_slots + split) * G + rg[i]; };
 
-  if (nloc == 0) {  // an empty split: m = -inf, l = 0, o = 0
+  if (nloc == 0) {  // an empty split: m = -inf, l = 0, o = 0 (no copies were issued)
     if (st == 0) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
@@ -270,15 +292,14 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
   for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float mu[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
   const uint4* qw = qs + mt * KS * 32 + lane;
-  int landed = 0;  // stream stages this warp saw land
   for (int k = 0; k < nk; ++k) {
-    const int sg = slot(k);
-    if (!mbar_wait(&full_bar[sg], (k / DEPTH) & 1)) {
-      if (lane == 0) set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
-      break;
-    }
+    // this thread's copies of stage k are done; past the stream's barrier so are its partner
+    // warp's, and both warps have read stage k - 1, whose slot takes stage k + DEPTH - 1
+    cp_async_wait<DEPTH - 2>();
+    stream_sync<MT>(st);
+    issue(k + DEPTH - 1);
 
-    landed = k + 1;
+    const int sg = slot(k);
     const uint8_t* kt = k_tiles + sg * C::kTile;
     const uint8_t* vt = v_tiles + sg * C::kTile;
     // K: token 8 nt + gid, codes tig * D/4 .. + D/4 (n-tile nt)
@@ -325,22 +346,6 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
         vr[t][0] = v.x;
         vr[t][1] = v.y;
       }
-    }
-    // Both tiles are read: the stage goes back.  The reads went through the generic
-    // proxy and the refill comes through the async proxy.
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty_bar[sg]);
-    // The loader refills the slot of the previous stage, which the other slice has released
-    // by now (or soon after).
-    if (loader && k >= 1 && issued < nk) {
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(&empty_bar[slot(k - 1)], ((k - 1) / DEPTH) & 1);
-      if (!__shfl_sync(kFull, ok, 0)) {
-        if (lane == 0) set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
-        break;
-      }
-      issue();
     }
 
     // ---- online softmax per row: the block max over the quad's 16 tokens
@@ -390,18 +395,11 @@ __global__ void __launch_bounds__(MmaPrefixCfg<D, MT>::kThreads, MmaPrefixCfg<D,
       mma16<true>(o[4 * i + 3], pa0, pa1, pa2, pa3, e4m3_hi(y01), e4m3_hi(y89));
     }
   }
-  // every copy the loader issued lands before the ring is reused as scratch (on the normal
-  // path this warp waited for all of them already)
-  if (loader && lane == 0) {
-    for (int k = landed; k < issued; ++k)
-      if (!mbar_wait(&full_bar[slot(k)], (k / DEPTH) & 1)) {
-        set_flag(p.status, PKV_DEVFLAG_WAIT_TIMEOUT);
-        break;
-      }
-  }
+  // the stages past the last one were empty groups: nothing is in flight once this returns
+  cp_async_wait<0>();
 
   // ================================================================ combine the streams
-  __syncthreads();  // the ring is drained: every issued copy landed and was read
+  __syncthreads();  // the ring is drained: every copy landed and was read
   float* scratch = reinterpret_cast<float*>(smem);  // [stream - 1][slice][kFrag][32 lanes]
   if (st > 0) {
     float* sc = scratch + ((st - 1) * MT + mt) * C::kFrag * 32 + lane;
@@ -533,8 +531,7 @@ int cascade_prefix_mma_ctas_per_sm(int device) {
 }
 
 template <int D, int MT>
-cudaError_t launch_cascade_prefix_mma(const CUtensorMap& tk, const CUtensorMap& tv, const PrefixParams& p, dim3 grid,
-                                      cudaStream_t stream, int device) {
+cudaError_t launch_cascade_prefix_mma(const PrefixParams& p, dim3 grid, cudaStream_t stream, int device) {
   using C = MmaPrefixCfg<D, MT>;
   cudaError_t e;
   if (prefix_mma_configure<D, MT>(device, &e) == 0) return e;
@@ -548,13 +545,12 @@ cudaError_t launch_cascade_prefix_mma(const CUtensorMap& tk, const CUtensorMap& 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, cascade_prefix_mma_kernel<D, MT>, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, cascade_prefix_mma_kernel<D, MT>, p);
 }
 
 #define PKV_DEFINE_PREFIX_MMA(D, MT)                                                                               \
   template int cascade_prefix_mma_ctas_per_sm<D, MT>(int);                                                        \
-  template cudaError_t launch_cascade_prefix_mma<D, MT>(const CUtensorMap&, const CUtensorMap&, const PrefixParams&, \
-                                                        dim3, cudaStream_t, int);
+  template cudaError_t launch_cascade_prefix_mma<D, MT>(const PrefixParams&, dim3, cudaStream_t, int);
 PKV_DEFINE_PREFIX_MMA(64, 1)
 PKV_DEFINE_PREFIX_MMA(64, 2)
 PKV_DEFINE_PREFIX_MMA(128, 1)

@@ -203,9 +203,9 @@ bool encode_kv_map_sw128(CUtensorMap* tm, void* base, int64_t num_blocks, int hk
   return r == CUDA_SUCCESS;
 }
 
-// The pool's E4M3 codes as boxes of 16 rows x D codes, swizzled so that the mma.sync prefix
-// pass reads its per-lane runs of codes without bank conflicts: the 128-byte swizzle for
-// 128-byte rows (D = 128), the 64-byte swizzle for 64-byte rows (D = 64).
+// The pool's E4M3 codes as boxes of 16 rows x D codes, swizzled so that the tensor-core
+// E4M3 decode reads its per-lane runs of codes without bank conflicts: the 128-byte swizzle
+// for 128-byte rows (D = 128), the 64-byte swizzle for 64-byte rows (D = 64).
 bool encode_kv_map_e4m3_swz(CUtensorMap* tm, void* base, int64_t num_blocks, int hkv, int d) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
                               static_cast<cuuint64_t>(num_blocks) * 16};
@@ -742,11 +742,10 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
 
   CUtensorMap tk, tv;
   const bool maps_ok =
-      mma_pass ? encode_kv_map_e4m3_swz(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim) &&
-                     encode_kv_map_e4m3_swz(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim)
-      : fp8 ? encode_kv_map(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim, true) &&
+      mma_pass ? true  // the mma.sync pass copies the codes without tensor maps
+      : fp8    ? encode_kv_map(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim, true) &&
                   encode_kv_map(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim, true)
-            : encode_kv_map_sw128(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim) &&
+               : encode_kv_map_sw128(&tk, cache->k_cache, cache->num_blocks, hkv, cache->head_dim) &&
                   encode_kv_map_sw128(&tv, cache->v_cache, cache->num_blocks, hkv, cache->head_dim);
   if (!maps_ok) return fail(PKV_ERR_INVALID_ARG, "cannot describe the KV pool as a TMA tensor map");
   pkv::PrefixParams pr{};
@@ -771,17 +770,19 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   pr.rec_slots = pp.pre_slots + sp.max_splits;
   pr.score_scale = softmax_scale * 1.4426950408889634f;  // log2(e)
   pr.scales = cache->scales;
+  pr.k_codes = static_cast<const uint8_t*>(cache->k_cache);
+  pr.v_codes = static_cast<const uint8_t*>(cache->v_cache);
   const dim3 pgrid(static_cast<unsigned>(pp.tiles), static_cast<unsigned>(hkv),
                    static_cast<unsigned>(px->num_prefixes * pp.pre_slots));
   const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   if (mma_pass) {
     if (cache->head_dim == 64)
-      e = mma_mt == 1 ? pkv::launch_cascade_prefix_mma<64, 1>(tk, tv, pr, pgrid, cs, device)
-                      : pkv::launch_cascade_prefix_mma<64, 2>(tk, tv, pr, pgrid, cs, device);
+      e = mma_mt == 1 ? pkv::launch_cascade_prefix_mma<64, 1>(pr, pgrid, cs, device)
+                      : pkv::launch_cascade_prefix_mma<64, 2>(pr, pgrid, cs, device);
     else
-      e = mma_mt == 1 ? pkv::launch_cascade_prefix_mma<128, 1>(tk, tv, pr, pgrid, cs, device)
-                      : pkv::launch_cascade_prefix_mma<128, 2>(tk, tv, pr, pgrid, cs, device);
+      e = mma_mt == 1 ? pkv::launch_cascade_prefix_mma<128, 1>(pr, pgrid, cs, device)
+                      : pkv::launch_cascade_prefix_mma<128, 2>(pr, pgrid, cs, device);
   } else if (cache->head_dim == 64)
     e = fp8 ? pkv::launch_cascade_prefix_tc<64, true>(tk, tv, pr, pgrid, cs, device)
             : pkv::launch_cascade_prefix_tc<64, false>(tk, tv, pr, pgrid, cs, device);

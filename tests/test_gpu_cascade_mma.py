@@ -128,7 +128,7 @@ def test_tcgen05_pass_on_the_same_inputs(pkv, defer):
 
 def test_repeated_calls_give_identical_bits(pkv):
     """Ten calls on the same inputs give the same bits: the streams of a slice combine in a
-    fixed order, and a ring stage goes back to the producer only after a proxy fence."""
+    fixed order, and a ring slot is refilled only after both warps of its stream have read it."""
     c, k8, v8, scales, q, full, lens = build_groups(2, 4, 128, [(8, 60), (7, 41)], seed=2400)
     kd, vd = k8.cuda(), v8.cuda()
     with env(PKV_PREFIX_PASS="mma", PKV_PREFIX_SPLIT_BLOCKS=12):
