@@ -39,6 +39,8 @@ def check_contract(d, steps, warmup):
     e2e = d["e2e"]
     assert e2e["unit"] == d["unit"] and 0 < e2e["value"] and e2e["h2d_bytes_per_step"] > 0
     assert e2e["d2h_bytes_per_step"] > 0
+    assert e2e["pipelined"] is True and e2e["serial"]["unit"] == d["unit"] and e2e["serial"]["value"] > 0
+    assert e2e["same_loop_without_copies_ms_per_step"] > 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1 and cb["sample"]
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
@@ -49,9 +51,10 @@ def test_bench_line_plain_decode():
     plus the read-only ceiling pass (one launch per timed step)."""
     d = run_bench("--config", "tiny", "--steps", "5", "--warmup", "3", "--cpu-seconds", "1", "--no-extra-configs")
     check_contract(d, 5, 3)
-    # fused step (1) + decode pass (append + decode: 2) + two-call pass (2) + e2e (the fused step
-    # and its two staging copies: 3), per step; the read pass
-    assert d["gpu_launches"] == (1 + 2 + 2 + 3) * 5 + 5
+    # fused step (1) + decode pass (append + decode: 2) + two-call pass (2) + serial e2e (the fused
+    # step and its two staging copies: 3) + pipelined e2e with and without its copies (the fused
+    # step; the copies are copy-engine transfers: 1 + 1), per step; the read pass
+    assert d["gpu_launches"] == (1 + 2 + 2 + 3 + 2) * 5 + 5
     assert d["two_call_step_us"] > 0 and "paged_append_decode" in d["step_call"]
     rc = d["read_ceiling"]
     assert rc["us"] > 0 and rc["gbs"] > 0 and abs(rc["frac"] - rc["gbs"] / d["roofline"]["peak"]) < 1e-3
@@ -64,8 +67,9 @@ def test_bench_line_cascade():
     d = run_bench("--config", "prefix_shared", "--cascade", "--steps", "3", "--warmup", "3", "--cpu-seconds", "1",
                   "--no-extra-configs")
     check_contract(d, 3, 3)
-    # append, prefix pass, decode, merge: three timed passes, the e2e one with two staging copies
-    assert d["gpu_launches"] == 4 * 3 * 3 + 2 * 3
+    # append, prefix pass, decode, merge: five timed passes (step, decode, serial e2e, pipelined
+    # e2e with and without its copies), the serial e2e one with two staging copies
+    assert d["gpu_launches"] == 4 * 3 * 5 + 2 * 3
     assert "cascade_prefix_tc_kernel" in d["roofline"]["kernel"]
 
 
