@@ -718,12 +718,23 @@ pkv_status pkv_cascade_decode_attention(const pkv_cache_desc* cache, const void*
   // The mma.sync pass (four per SM fit): two per SM, so that decode CTAs stream the sequences'
   // own blocks beside it (fork step 55.7 -> 53.8 us).
   int plan_per_sm = mma_pass ? std::min(per_sm, 2) : (fp8 ? per_sm : 1);
+  long long plan_slots = static_cast<long long>(dev->sm_count) * plan_per_sm;
   if (const char* env = std::getenv("PKV_PREFIX_CTAS_PER_SM")) {
     const long v = std::strtol(env, nullptr, 10);
-    if (v >= 1 && v <= per_sm) plan_per_sm = static_cast<int>(v);
+    if (v >= 1 && v <= per_sm) plan_slots = static_cast<long long>(dev->sm_count) * v;
+  } else if (!fp8) {
+    // bf16 pools, where the pass runs beside the decode: when the pass's work (128-row tiles
+    // x prefix blocks) is under half the decode's (sequences x kv heads x half the longest
+    // context, in blocks), it is planned for half the SMs, so its splits are fewer and longer
+    // and the decode keeps more of the GPU (shared-prefix step 75.9-76.8 -> 72.7 us); a
+    // prefix-heavy call keeps every SM for the pass, which is then the longer part
+    const long long tiles = (static_cast<long long>(px->max_members) * g + 127) / 128;
+    const long long pass_work = static_cast<long long>(px->num_prefixes) * tiles * hkv *
+                                ((static_cast<long long>(px->max_prefix_len) + 15) / 16);
+    const long long dec_work = static_cast<long long>(batch) * hkv * ((static_cast<long long>(max_context_len) + 15) / 16) / 2;
+    if (2 * pass_work < dec_work) plan_slots = std::max(1LL, plan_slots / 2);
   }
-  PrefixPlan pp = plan_prefix(px->num_prefixes, px->max_members, px->max_prefix_len, g, hkv,
-                              static_cast<long long>(dev->sm_count) * plan_per_sm);
+  PrefixPlan pp = plan_prefix(px->num_prefixes, px->max_members, px->max_prefix_len, g, hkv, plan_slots);
   if (mma_pass) pp.tiles = 1;
   if (static_cast<long long>(px->num_prefixes) * pp.pre_slots > 65535 || pp.tiles > 0x7fffffff / 2)
     return fail(PKV_ERR_UNSUPPORTED, "too many prefixes for the prefix-pass grid");
