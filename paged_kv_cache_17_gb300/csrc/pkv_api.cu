@@ -451,16 +451,26 @@ size_t pkv_cascade_workspace_size(int32_t batch, int32_t num_q_heads, int32_t nu
                                     : pkv::cascade_prefix_mma_ctas_per_sm<128, 2>(device)),
                          1};
   per_sm[3] = std::min(per_sm[2], 2);  // the mma.sync pass as the cascade call plans it
-  PrefixPlan pp{0, 0, 0};
+  int max_per_sm = 1;
   for (int k = 0; k < 4; ++k) {
     if (per_sm[k] <= 0) {
       fail(PKV_ERR_CUDA, "the prefix pass does not fit on an SM of this device");
       return 0;
     }
-    const PrefixPlan pk = plan_prefix(num_prefixes, max_members, max_prefix_len, num_q_heads / num_kv_heads,
-                                      num_kv_heads, static_cast<long long>(dev->sm_count) * per_sm[k]);
-    if (pk.pre_slots > pp.pre_slots) pp = pk;
+    max_per_sm = std::max(max_per_sm, per_sm[k]);
   }
+  // every slot count the call can plan with: a whole number of CTAs per SM up to what any
+  // pass fits (the plan or PKV_PREFIX_CTAS_PER_SM), and half of it (bf16 passes small next to
+  // their decode); the split count is not monotonic in the slots, so all of them are tried
+  PrefixPlan pp{0, 0, 0};
+  for (int v = 1; v <= max_per_sm; ++v)
+    for (int half = 0; half < 2; ++half) {
+      long long slots = static_cast<long long>(dev->sm_count) * v;
+      if (half) slots = std::max(1LL, slots / 2);
+      const PrefixPlan pk = plan_prefix(num_prefixes, max_members, max_prefix_len, num_q_heads / num_kv_heads,
+                                        num_kv_heads, slots);
+      if (pk.pre_slots > pp.pre_slots) pp = pk;
+    }
   Split sp;
   WsLayout ws;
   Variant var;
