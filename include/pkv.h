@@ -269,7 +269,8 @@ pkv_status pkv_paged_decode_attention_noalloc(const pkv_cache_desc* cache, const
  *   each weight's relative error is at most 2^-11).
  *   Tuning (environment, read at each call; results agree within the tolerances above):
  *   PKV_PREFIX_SPLIT_BLOCKS (>= 4) fixes the prefix blocks per split of the prefix pass,
- *   PKV_PREFIX_CTAS_PER_SM (1 or 2) the prefix-pass CTAs an SM is planned for, and
+ *   PKV_PREFIX_CTAS_PER_SM (1 up to the pass's CTAs that fit an SM) the prefix-pass CTAs an SM
+ *   is planned for, and
  *   PKV_CASCADE_DEFER (0 or 1) whether the prefix records are merged in the decode kernel (0)
  *   or by the merge kernel after it (1), and PKV_PREFIX_PASS ("tc" or "mma") which prefix
  *   pass runs where both apply; PKV_SPLIT_TOKENS applies as for the plain decode.
